@@ -1,0 +1,415 @@
+"""Benchmark of the varlen ViT attention hot path on GB300.
+
+One step = the whole path over one packed batch: the 2D RoPE table and
+positions (vit_rope_freqs), the fused QK-RMSNorm + RoPE prologue
+(vit_qk_norm_rope) and the segment-aware varlen attention (vit_varlen_attn,
+scheduler + attention kernels). Metric: useful attention TFLOP/s,
+4 * sum(L_i^2) * H * D per step (cross-segment blocks and tile padding are not
+counted), plus tokens/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
+
+Prints one JSON line (rank 0). With N > 1 (launched by torchrun) every rank
+runs its own replica of the batch: there is no exchange on this path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from vision_encoder_varlen_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "varlen ViT attention TFLOP/s (4·ΣLi²·H·D) and tokens/s on 1 GB300; % of BF16 peak"
+L2_BYTES = 129 * 2 ** 20
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ clocks during the timed region
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = max(mx, float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        load = [s for s in sm if s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ the GPU arm
+
+class Path:
+    """Device-resident buffers and the three calls of one step."""
+
+    def __init__(self, vit, w: wl.Workload, t: dict, device):
+        self.vit, self.w = vit, w
+        T, H, D, B = w.total_tokens, w.heads, w.head_dim, w.num_segments
+        self.grid = torch.from_numpy(w.grid_hw.copy()).to(device)
+        self.q, self.k, self.v = (t[n].to(device) for n in ("q", "k", "v"))
+        self.nw = t["norm_w"].to(device) if t["norm_w"] is not None else None
+        self.qr = torch.empty_like(self.q)
+        self.kr = torch.empty_like(self.k)
+        self.out = torch.empty_like(self.q)
+        self.ws = torch.empty(vit.workspace_size(T, H, B, D), dtype=torch.uint8, device=device)
+        self.status = vit.new_status(device)
+
+    def step(self):
+        vit, w = self.vit, self.w
+        inv_freq, pos, cu = vit.rope_freqs(self.grid, w.total_tokens, w.head_dim, w.theta, status=self.status)
+        vit.qk_norm_rope(self.q, self.k, pos, inv_freq, self.nw, w.eps, q_out=self.qr, k_out=self.kr)
+        vit.varlen_attn(self.qr, self.kr, self.v, cu, w.max_seqlen, out=self.out, workspace=self.ws,
+                        status=self.status)
+
+
+def e2e_step(vit, w, host, device, stream):
+    """Through the public API from pinned host buffers: H2D inputs, the three calls, D2H output."""
+    grid = host["grid"].to(device, non_blocking=True)
+    q = host["q"].to(device, non_blocking=True)
+    k = host["k"].to(device, non_blocking=True)
+    v = host["v"].to(device, non_blocking=True)
+    nw = host["nw"].to(device, non_blocking=True) if host["nw"] is not None else None
+    inv_freq, pos, cu = vit.rope_freqs(grid, w.total_tokens, w.head_dim, w.theta)
+    qr, kr = vit.qk_norm_rope(q, k, pos, inv_freq, nw, w.eps, inplace=True)
+    out = vit.varlen_attn(qr, kr, v, cu, w.max_seqlen)
+    host["out"].copy_(out, non_blocking=True)
+
+
+def load_traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel, {})
+    src = e.get("source")
+    if not src or e.get("workload") != workload:
+        return None
+    with open(os.path.join(ROOT, src), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != e.get("source_sha256_16"):
+            return None
+    return e.get("bytes_per_launch")
+
+
+def kernel_algorithmic_flops(w: wl.Workload, kernel: str) -> float:
+    """Useful flops a kernel processes per step: 4 L^2 H D over the segments it owns."""
+    L = w.lengths.astype(np.float64)
+    short_max = SHORT_MAX_BY_KERNEL.get(kernel)
+    if short_max is not None:
+        L = L[L <= short_max] if kernel == "attn_short" else L[L > short_max]
+    return float(4.0 * np.sum(L * L) * w.heads * w.head_dim)
+
+
+SHORT_MAX_BY_KERNEL = {"attn_short": float("inf"), "attn_long": float("inf")}
+
+
+def cpu_baseline_sample(w: wl.Workload, t: dict, target_s: float):
+    """The fp64 oracle, as it stands, on a bounded sample: the first query rows of
+    the longest image (all heads, all its keys), grown until ~target_s of CPU work."""
+    import oracle
+    bits = [wl.bf16_bits(t[n]) for n in ("q", "k", "v")]
+    nw = wl.bf16_bits(t["norm_w"]) if t["norm_w"] is not None else None
+    cu = w.cu_seqlens
+    seg = int(np.argmax(w.lengths))
+    a, L = int(cu[seg]), int(w.lengths[seg])
+    rows_n, spent, flops, calls = 4, 0.0, 0.0, 0
+    t_start = time.perf_counter()
+    while spent < target_s:
+        n = min(rows_n, L)
+        rows = np.arange(a, a + n)
+        t0 = time.perf_counter()
+        oracle.full_path(w.grid_hw, *bits, nw, w.eps, w.theta, rows=rows)
+        dt = time.perf_counter() - t0
+        spent += dt
+        flops += 4.0 * n * L * w.heads * w.head_dim
+        calls += 1
+        if dt < target_s / 8:
+            rows_n *= 2
+    wall = time.perf_counter() - t_start
+    return {"value": flops / wall / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{calls} oracle calls over query rows [first {rows_n} max] of the {L}-token image, all "
+                      f"{w.heads} heads and all its keys (RoPE/norm of every token included), {wall:.1f} s wall",
+            "seconds": wall, "useful_flops": flops}
+
+
+def run_ours(args, rank, world, local):
+    import vision_encoder_varlen_gb300 as vit
+    from vision_encoder_varlen_gb300 import _build
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = wl.make_config(args.config)
+    t = w.tensors()
+    T, H, D = w.total_tokens, w.heads, w.head_dim
+    path = Path(vit, w, t, device)
+    stream = torch.cuda.current_stream()
+    tensor_bytes = T * H * D * 2
+    working_set = 6 * tensor_bytes
+    flush = working_set < 2 * L2_BYTES
+    flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device) if flush else None
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        path.step()
+    torch.cuda.synchronize()
+    code = vit.read_status(path.status)
+    if code != 0:
+        raise RuntimeError(f"device status {code}: {vit.status_string(code)}")
+
+    # ---- timed region: K steps, per-kernel CUDA events recorded live on the launch stream
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = vit.launch_count()
+    vit.kernel_timing_read()
+    with ClockSampler(local) as clocks:
+        vit.kernel_timing(True)
+        if not flush:
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(args.steps):
+                path.step()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            total_ms = ev0.elapsed_time(ev1)
+        else:
+            total_ms = 0.0
+            for _ in range(args.steps):
+                flush_buf.zero_()
+                ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ev0.record(stream)
+                path.step()
+                ev1.record(stream)
+                torch.cuda.synchronize()
+                total_ms += ev0.elapsed_time(ev1)
+        vit.kernel_timing(False)
+        kt = vit.kernel_timing_read()
+    torch.cuda.synchronize()
+    barrier()
+    launches = vit.launch_count() - launches0
+    ms = total_ms / args.steps
+    if world > 1:
+        m = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(m, op=torch.distributed.ReduceOp.MAX)
+        ms = float(m.item())
+    clk = clocks.summary()
+
+    # ---- end to end through the public API from pinned host memory
+    host = {"grid": torch.from_numpy(w.grid_hw.copy()).pin_memory(),
+            "q": t["q"].pin_memory(), "k": t["k"].pin_memory(), "v": t["v"].pin_memory(),
+            "nw": t["norm_w"].pin_memory() if t["norm_w"] is not None else None,
+            "out": torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory()}
+    h2d = 3 * tensor_bytes + host["grid"].numel() * 4 + (host["nw"].numel() * 2 if host["nw"] is not None else 0)
+    d2h = tensor_bytes
+    for _ in range(2):
+        e2e_step(vit, w, host, device, stream)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step(vit, w, host, device, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        m = torch.tensor([e2e_ms], device=device)
+        torch.distributed.all_reduce(m, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(m.item())
+
+    if rank != 0:
+        return
+    peaks, peaks_src = load_peaks()
+    flops = w.useful_flops
+    value = flops * world / (ms * 1e-3) / 1e12
+    kernels = {name: {"launches": n, "avg_ms": tot / max(n, 1)} for name, (n, tot) in kt.items()}
+    dom = max(kt.items(), key=lambda kv: kv[1][1])[0] if kt else None
+    roofline = None
+    if dom is not None:
+        n, tot = kt[dom]
+        avg_s = tot / n * 1e-3
+        if dom.startswith("attn"):
+            alg = kernel_algorithmic_flops(w, dom)
+            peak = peaks["bf16_tflops_sustained"]
+            achieved = alg / avg_s / 1e12
+            roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak, "traffic": load_traffic(dom, w.name),
+                        "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside a long step loop)",
+                        "algorithmic_flops_per_launch": alg}
+        else:
+            alg = 8.0 * T * H * D if dom == "qk_norm_rope" else 8.0 * T
+            achieved = alg / avg_s / 1e9
+            roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(dom, w.name),
+                        "peak_source": f"{peaks_src} hbm_gbs"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": T, "segments": w.num_segments, "heads": H, "head_dim": D,
+                   "qk_norm": w.qk_norm, "max_seqlen": w.max_seqlen, "useful_flops_per_step": flops,
+                   "l2": "L2 flushed between steps" if flush else
+                   f"inputs larger than L2 ({working_set / 2 ** 20:.0f} MiB working set)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "tokens_per_s": T * world / (ms * 1e-3),
+        "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
+        "clocks": clk,
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "kernels": kernels,
+        "roofline": roofline,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(w, t, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores; each
+    step is a bounded sample (query rows of the longest image, all heads)."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = wl.make_config(args.config)
+    t = w.tensors()
+    bits = [wl.bf16_bits(t[n]) for n in ("q", "k", "v")]
+    nw = wl.bf16_bits(t["norm_w"]) if t["norm_w"] is not None else None
+    seg = int(np.argmax(w.lengths))
+    a, L = int(w.cu_seqlens[seg]), int(w.lengths[seg])
+    n = max(1, min(L, args.ref_rows))
+    rows = np.arange(a, a + n)
+    for _ in range(args.warmup):
+        oracle.full_path(w.grid_hw, *bits, nw, w.eps, w.theta, rows=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.full_path(w.grid_hw, *bits, nw, w.eps, w.theta, rows=rows)
+    wall = time.perf_counter() - t0
+    flops = 4.0 * n * L * w.heads * w.head_dim
+    value = flops * args.steps / wall / 1e12
+    sample = f"{n} query rows of the {L}-token image per step, all {w.heads} heads and all its keys"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.total_tokens, "segments": w.num_segments, "heads": w.heads,
+                   "head_dim": w.head_dim, "qk_norm": w.qk_norm, "max_seqlen": w.max_seqlen},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=16)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

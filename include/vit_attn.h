@@ -1,0 +1,205 @@
+/*
+ * vit_attn.h -- C ABI of the GB300 (sm_103a) varlen ViT encoder attention library.
+ *
+ * The hot path of a multimodal vision encoder's attention layer: several images
+ * packed into one token stream delimited by cu_seqlens, every token attending
+ * only to the tokens of its own image, after 2D vision RoPE and optional
+ * per-head Q/K RMSNorm.
+ *
+ * Sources of the operations (web pages):
+ *   [Dots]  vLLM docs, vllm.models.dots3_note.nvidia.vision_attention:
+ *           VisionAttention (dense block-diagonal mask), VisionAttentionV2
+ *           (per-segment loop), VisionRotaryEmbedding, _RMSNorm,
+ *           _VisionAttentionBase._qkv_with_rope.
+ *   [TS]    tokenspeed mm_encoder_attention.py: _varlen_metadata, the varlen
+ *           backends, MultimodalEncoderAttention.forward (cos/sin duplication).
+ *
+ * Conventions shared by every call:
+ *   - All pointers named *_dev or documented "device" are CUDA device pointers
+ *     on the current device. The caller owns every buffer; the library never
+ *     allocates or frees device memory and keeps no device state between
+ *     calls.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and never
+ *     synchronise, except vit_read_status and vit_kernel_timing_read.
+ *   - bf16 tensors are raw 16-bit bfloat16 values ("const void*"), row-major,
+ *     laid out [T, H, D] with a caller-given token stride (in elements) and a
+ *     head stride of exactly D. Strides of 3*H*D (packed qkv views) are fine.
+ *   - Errors the host can see (null pointers, bad sizes, strides, alignment,
+ *     a too-small workspace) return a negative vit_status_t at once and launch
+ *     nothing. Errors only the device can see (malformed cu_seqlens, a segment
+ *     longer than max_seqlen, a grid that does not sum to T, a wait that timed
+ *     out) are written into *status_dev when status_dev is non-NULL: kernels
+ *     only ever store a negative code there and the first error wins, so the
+ *     caller zeroes the word once and reads it with vit_read_status. On a
+ *     device-detected error the affected call computes nothing and leaves its
+ *     outputs untouched. No kernel traps or waits without a bound.
+ */
+#ifndef VIT_ATTN_H
+#define VIT_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *vit_stream_t; /* same type as cudaStream_t */
+typedef int vit_status_t;
+
+enum {
+    VIT_OK = 0,
+    VIT_ERR_NULL_POINTER = -1,       /* a required pointer is NULL */
+    VIT_ERR_BAD_HEAD_DIM = -2,       /* head_dim not in {32, 64, 80, 96, 128} */
+    VIT_ERR_BAD_SHAPE = -3,          /* T < 0, H < 1, B < 1, T too large, ... */
+    VIT_ERR_BAD_STRIDE = -4,         /* token stride < H*D or not a multiple of 8 elements */
+    VIT_ERR_MISALIGNED = -5,         /* a tensor pointer is not 16-byte aligned */
+    VIT_ERR_WORKSPACE_TOO_SMALL = -6,/* workspace smaller than vit_varlen_attn_workspace_size */
+    VIT_ERR_TOO_MANY_SEGMENTS = -7,  /* B (or n_img) above VIT_MAX_SEGMENTS */
+    VIT_ERR_CUDA = -8,               /* a CUDA runtime call failed (launch, attribute, ...) */
+    VIT_ERR_UNSUPPORTED_DEVICE = -9, /* current device is not compute capability 10.3 */
+    VIT_ERR_BAD_SEQLENS = -10,       /* device: cu[0] != 0, cu decreasing, or cu[B] != T */
+    VIT_ERR_SEQLEN_EXCEEDS_MAX = -11,/* device: some segment longer than max_seqlen */
+    VIT_ERR_GRID_MISMATCH = -12,     /* device: sum of h*w over the grid != T, or h, w < 0 */
+    VIT_ERR_TIMEOUT = -13,           /* device: a bounded wait inside a kernel gave up */
+    VIT_ERR_BAD_ARGUMENT = -14       /* any other invalid scalar argument */
+};
+
+#define VIT_MAX_SEGMENTS 8192
+
+/* Library version string (never NULL). */
+const char *vit_version(void);
+
+/* Human-readable text of a status code (never NULL). */
+const char *vit_status_string(vit_status_t status);
+
+/* VIT_OK when `device` is a compute capability 10.3 GPU this library was built for. */
+vit_status_t vit_device_supported(int device);
+
+/*
+ * 2D vision RoPE frequency table and patch positions.
+ *
+ * [Dots] VisionRotaryEmbedding(dim, theta): inv_freq[j] = 1 / theta^(2j/dim)
+ * for j < dim/2, in fp32; _compute_freqs multiplies positions 0..seqlen-1 by
+ * it. For 2D RoPE the table is built with dim = head_dim/2 and used once for
+ * the row position and once for the column position of every patch.
+ *
+ *   dim         rotary table dimension = head_dim / 2 (even, >= 2, <= 256).
+ *   theta       base (10000 in the Dots and tokenspeed encoders); > 0.
+ *   grid_hw     device int32 [n_img, 2]: patch grid (h, w) of each image, in
+ *               packing order.
+ *   n_img       number of images, 0 <= n_img <= VIT_MAX_SEGMENTS.
+ *   T           total tokens the caller packed; must equal sum(h*w) (checked
+ *               on the device, VIT_ERR_GRID_MISMATCH otherwise).
+ *   inv_freq    device fp32 [dim/2] output, or NULL.
+ *   pos_hw      device int32 [T, 2] output, or NULL: (row, col) of each token
+ *               inside its image, row-major (col fastest), restarting at 0 for
+ *               every image.
+ *   cu_seqlens  device int32 [n_img + 1] output, or NULL: 0, h0*w0, ... (the
+ *               offsets VisionAttention and the varlen backends take).
+ *   status_dev  device int32 [1] or NULL (see conventions).
+ */
+vit_status_t vit_rope_freqs(int dim, float theta, const int32_t *grid_hw, int n_img, int64_t T,
+                            float *inv_freq, int32_t *pos_hw, int32_t *cu_seqlens,
+                            int32_t *status_dev, vit_stream_t stream);
+
+/*
+ * Fused QK-RMSNorm + 2D rotate-half RoPE prologue (one pass over q and k).
+ *
+ * [Dots] _RMSNorm: y = bf16(fp32(x) * rsqrt(mean(fp32(x)^2) + eps)) * weight,
+ * applied to q with the q weight and to k with the k weight
+ * (_VisionAttentionBase._qkv_with_rope), then RoPE. [TS] forward duplicates a
+ * half-width cos/sin table over both halves of the head (rotate-half / NeoX
+ * layout). For m < D/2 with angle a_m = row * inv_freq[m] (m < D/4) or
+ * col * inv_freq[m - D/4] (m >= D/4):
+ *   y[m]       = x[m] cos a_m - x[m + D/2] sin a_m
+ *   y[m + D/2] = x[m + D/2] cos a_m + x[m] sin a_m
+ * computed in fp32 and rounded to bf16 once.
+ *
+ *   q_in, k_in     device bf16 [T, H, D], token strides q_in_stride, k_in_stride.
+ *   q_out, k_out   device bf16 [T, H, D], token strides q_out_stride,
+ *                  k_out_stride; may equal q_in / k_in (in place, same stride).
+ *   pos_hw         device int32 [T, 2] from vit_rope_freqs.
+ *   inv_freq       device fp32 [D/4] from vit_rope_freqs(dim = D/2).
+ *   norm_w         device bf16 [2, D] (row 0 = q weight, row 1 = k weight), or
+ *                  NULL for no QK-norm.
+ *   eps            RMSNorm epsilon (>= 0), added inside the rsqrt.
+ * D must be in {32, 64, 80, 96, 128}; pointers 16-byte aligned; strides
+ * multiples of 8 elements and >= H*D.
+ */
+vit_status_t vit_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, void *k_out,
+                              int64_t T, int H, int D,
+                              int64_t q_in_stride, int64_t q_out_stride,
+                              int64_t k_in_stride, int64_t k_out_stride,
+                              const int32_t *pos_hw, const float *inv_freq,
+                              const void *norm_w, float eps, vit_stream_t stream);
+
+/*
+ * Workspace bytes vit_varlen_attn needs for these sizes (an upper bound
+ * independent of the segment lengths). Returns 0 for invalid sizes.
+ */
+size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D);
+
+/*
+ * Non-causal variable-length packed multi-head attention.
+ *
+ * [Dots] VisionAttention / VisionAttentionV2: for each segment i of the packed
+ * stream, rows [cu[i], cu[i+1]), and each head h:
+ *   out[t, h, :] = softmax_j(scale * <q[t, h], k[j, h]>) v[j, h], j in segment i
+ * (a block-diagonal mask; no token ever attends across segments), softmax in
+ * fp32, bf16 inputs, fp32 accumulation, bf16 output.
+ *
+ *   q, k, v       device bf16 [T, H, D], token strides q_stride, k_stride, v_stride.
+ *   cu_seqlens    device int32 [B + 1] segment offsets, or NULL for B uniform
+ *                 segments of T/B tokens ([TS] _varlen_metadata); zero-length
+ *                 segments are allowed. Validated on the device.
+ *   B             number of segments, 1 <= B <= VIT_MAX_SEGMENTS.
+ *   max_seqlen    an upper bound on the segment lengths (may be padded to a
+ *                 CUDA-graph bucket, [TS] round_up_to_bucket); a segment longer
+ *                 than it is a device error. Used for validation only.
+ *   scale         softmax scale; <= 0 selects 1/sqrt(D) ([TS] head_size**-0.5).
+ *   out           device bf16 [T, H, D] with token stride out_stride (the
+ *                 [T, H*D] layout the output projection takes).
+ *   workspace     device scratch of >= vit_varlen_attn_workspace_size(T, H, B, D)
+ *                 bytes, 16-byte aligned, owned by the caller, overwritten by
+ *                 every call (calls sharing one workspace must not overlap).
+ * D must be in {32, 64, 80, 96, 128}; T < 2^31.
+ */
+vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                             int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                             const int32_t *cu_seqlens, int B, int max_seqlen, float scale,
+                             void *out, int64_t out_stride, void *workspace, size_t workspace_bytes,
+                             int32_t *status_dev, vit_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read the status word. Returns VIT_OK, the first
+ * device-detected error code stored there, or VIT_ERR_CUDA when the stream or
+ * the copy failed. The only call of the compute path that blocks the host.
+ */
+vit_status_t vit_read_status(const int32_t *status_dev, vit_stream_t stream);
+
+/* ---- instrumentation (benchmarks and tests) ---- */
+
+/* Total number of kernels this library has launched since it was loaded. */
+int64_t vit_launch_count(void);
+
+typedef struct {
+    const char *name;   /* kernel name (static string) */
+    int64_t launches;   /* launches recorded since the last read */
+    double total_ms;    /* sum of their device durations (CUDA events on the launch stream) */
+} vit_kernel_time_t;
+
+/* Turn per-launch CUDA-event timing of every kernel on (1) or off (0). Returns the previous state. */
+int vit_kernel_timing(int enable);
+
+/*
+ * Wait for the recorded events, aggregate per kernel name into out[0..max_entries),
+ * clear the record, and return the number of entries written (< 0 on error).
+ */
+int vit_kernel_timing_read(vit_kernel_time_t *out, int max_entries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VIT_ATTN_H */

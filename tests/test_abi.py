@@ -1,0 +1,113 @@
+"""The C-ABI library: it builds, loads without a GPU, exports every declared
+symbol, and rejects host-detectable bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import vision_encoder_varlen_gb300 as vit
+from vision_encoder_varlen_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vit_attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return vit.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(vit_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("vit_rope_freqs", "vit_qk_norm_rope", "vit_varlen_attn"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings(L):
+    assert vit.status_string(0) == "ok"
+    for code in range(-1, -15, -1):
+        s = vit.status_string(code)
+        assert s and s != "unknown status", code
+    assert vit.status_string(-999) == "unknown status"
+    assert "sm_103a" in vit.version()
+
+
+def test_workspace_size_bounds(L):
+    # header + one 16-byte item per (head, 64-row block) plus one per segment and head
+    assert vit.workspace_size(1024, 16, 1, 80) == 64 + 16 * 16 * (16 + 1)
+    assert vit.workspace_size(0, 4, 0, 32) == 64
+    assert vit.workspace_size(100, 4, 2, 81) == 0        # bad head_dim
+    assert vit.workspace_size(100, 0, 2, 80) == 0        # no heads
+    assert vit.workspace_size(100, 4, 8193, 80) == 0     # too many segments
+
+
+def _attn(L, **kw):
+    args = dict(q=8, k=8, v=8, T=128, H=2, D=80, qs=160, ks=160, vs=160, cu=16, B=1, max_seqlen=128, scale=0.0,
+                out=8, os=160, ws=256, ws_bytes=1 << 20, status=None, stream=None)
+    args.update(kw)
+    a = args
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return L.vit_varlen_attn(p(a["q"] * 16 if a["q"] else None), p(a["k"] * 16 if a["k"] else None),
+                             p(a["v"] * 16 if a["v"] else None), a["T"], a["H"], a["D"], a["qs"], a["ks"], a["vs"],
+                             p(a["cu"]), a["B"], a["max_seqlen"], a["scale"], p(a["out"] * 16 if a["out"] else None),
+                             a["os"], p(a["ws"]), a["ws_bytes"], p(a["status"]), p(a["stream"]))
+
+
+def test_host_validation_without_gpu(L):
+    # every case below fails a host check, so nothing reaches the CUDA runtime
+    assert _attn(L, D=81) == -2
+    assert _attn(L, H=0) == -3
+    assert _attn(L, T=-1) == -3
+    assert _attn(L, B=9000) == -7
+    assert _attn(L, B=0) == -3                      # T > 0 but no segment
+    assert _attn(L, qs=100) == -4                   # stride < H*D
+    assert _attn(L, ks=164) == -4                   # stride not a multiple of 8
+    assert _attn(L, q=0) == -1
+    assert _attn(L, ws=0) == -1
+    assert _attn(L, ws=264) == -5                   # workspace misaligned
+    assert _attn(L, ws_bytes=64) == -6
+    assert _attn(L, max_seqlen=0) == -14
+    assert _attn(L, scale=float("nan")) == -14
+    assert _attn(L, cu=0, B=3) == -14               # uniform split needs T % B == 0
+    assert _attn(L, T=0, B=0) == 0                  # nothing to do
+
+
+def test_prologue_and_rope_validation_without_gpu(L):
+    p = ctypes.c_void_p
+    assert L.vit_qk_norm_rope(p(16), p(16), p(16), p(16), 10, 2, 72, 144, 144, 144, 144, p(16), p(16), None,
+                              1e-6, None) == -2
+    assert L.vit_qk_norm_rope(None, p(16), p(16), p(16), 10, 2, 80, 160, 160, 160, 160, p(16), p(16), None,
+                              1e-6, None) == -1
+    assert L.vit_qk_norm_rope(p(16), p(16), p(16), p(16), 10, 2, 80, 160, 160, 160, 160, p(16), p(16), None,
+                              -1.0, None) == -14
+    assert L.vit_qk_norm_rope(p(16), p(32), p(16), p(16), 10, 2, 80, 160, 160, 168, 160, p(16), p(16), None,
+                              1e-6, None) == -4  # in-place k with different strides
+    assert L.vit_qk_norm_rope(p(16), p(16), p(16), p(16), 0, 2, 80, 160, 160, 160, 160, None, None, None,
+                              1e-6, None) == 0   # empty: nothing to do
+    assert L.vit_rope_freqs(3, 10000.0, p(16), 1, 4, p(16), p(16), p(16), None, None) == -14   # odd dim
+    assert L.vit_rope_freqs(40, -1.0, p(16), 1, 4, p(16), p(16), p(16), None, None) == -14     # theta <= 0
+    assert L.vit_rope_freqs(40, 10000.0, None, 1, 4, p(16), p(16), p(16), None, None) == -1
+    assert L.vit_rope_freqs(40, 10000.0, p(16), 9000, 4, p(16), p(16), p(16), None, None) == -7
+    assert L.vit_rope_freqs(40, 10000.0, p(16), 1, 4, None, None, None, None, None) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import importlib
+    monkeypatch.setattr(vit, "_lib", None)
+    monkeypatch.setattr(vit, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        vit.lib()

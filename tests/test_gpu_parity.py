@@ -1,0 +1,138 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle
+on the same seeded inputs (bf16 widened exactly)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import vision_encoder_varlen_gb300 as vit
+from vision_encoder_varlen_gb300 import _build
+from vision_encoder_varlen_gb300 import workloads as wl
+from helpers import MAX_ABS, MEAN_ABS, assert_close, gpu_full_path, sample_rows, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _build.build()
+    assert vit.lib().vit_device_supported(torch.cuda.current_device()) == 0, "not an sm_103 device"
+
+
+def test_native_library_is_loaded():
+    vit.lib()
+    maps = open("/proc/self/maps").read()
+    assert vit.LIB_PATH in maps
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+def test_rope_freqs_exact(idx):
+    w = wl.make_config(idx)
+    status = vit.new_status()
+    grid = torch.from_numpy(w.grid_hw.copy()).cuda()
+    inv_freq, pos, cu = vit.rope_freqs(grid, w.total_tokens, w.head_dim, w.theta, status=status)
+    assert vit.read_status(status) == 0
+    cu_ref, pos_ref = oracle.grid_positions(w.grid_hw)
+    assert np.array_equal(cu.cpu().numpy(), cu_ref)                       # bit-exact
+    assert np.array_equal(pos.cpu().numpy(), pos_ref)                     # bit-exact
+    # fp32 table (the page builds it in float32) against the fp64 closed form
+    np.testing.assert_allclose(inv_freq.cpu().numpy(), oracle.rope_inv_freq(w.head_dim // 2, w.theta),
+                               rtol=1e-6, atol=0)
+
+
+def _prologue_bound(ref: np.ndarray) -> np.ndarray:
+    """Per-element bound for bf16 prologue outputs.
+
+    GPU: bf16(x*rsqrt) and bf16(.*w) each round once (relative 2^-9), the fp32
+    rotation of a pair (a, b) rounds once more to bf16. With |a|+|b| <= sqrt(2)*r
+    (r = the pair norm, preserved by the rotation) the error is below
+    (2*2^-9*sqrt(2) + 2^-9) * r ~= 2^-7 * r; fp32 angle and powf/sincosf errors
+    add < 1e-4 * r for positions < 1000. Bound used: 2^-7 * r + 1e-5.
+    """
+    D = ref.shape[-1]
+    r = np.sqrt(ref[..., : D // 2] ** 2 + ref[..., D // 2:] ** 2)
+    r = np.concatenate([r, r], axis=-1)
+    return 2.0 ** -7 * r + 1e-5
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+def test_prologue_parity(idx):
+    w = wl.make_config(idx)
+    t = w.tensors()
+    _, qr, kr, _, _, _ = gpu_full_path(w, t)
+    torch.cuda.synchronize()
+    _, pos = oracle.grid_positions(w.grid_hw)
+    nw = None if t["norm_w"] is None else wl.bf16_bits(t["norm_w"])
+    for name, got, wrow in (("q", qr, 0), ("k", kr, 1)):
+        ref = oracle.norm_rope(wl.bf16_bits(t[name]), pos, w.theta, None if nw is None else nw[wrow],
+                               w.qk_norm, w.eps)
+        g = to_f64(got)
+        bound = _prologue_bound(ref)
+        bad = np.abs(g - ref) > bound
+        assert not bad.any(), f"{name}: {bad.sum()} elements outside the bf16 bound, worst " \
+                              f"{np.max(np.abs(g - ref) - bound):.3e}"
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_full_path_parity(idx):
+    w = wl.make_config(idx)
+    t = w.tensors()
+    status = vit.new_status()
+    out, *_ = gpu_full_path(w, t, status=status)
+    assert vit.read_status(status) == 0
+    ref = oracle.full_path(w.grid_hw, *(wl.bf16_bits(t[n]) for n in ("q", "k", "v")),
+                           None if t["norm_w"] is None else wl.bf16_bits(t["norm_w"]), w.eps, w.theta)
+    assert_close(out, ref, what=w.name)
+
+
+def test_full_path_parity_mixed_long_short_sampled():
+    """The 256x256 + 7 small images case at full size: all rows of the small
+    images, and 256 rows of the 65536-token image (first/last/tile-boundary
+    rows plus a seeded random set), every head."""
+    w = wl.make_config(5)
+    t = w.tensors()
+    status = vit.new_status()
+    out, *_ = gpu_full_path(w, t, status=status)
+    assert vit.read_status(status) == 0
+    rows = sample_rows(w, big_rows=256, seed=5)
+    ref = oracle.full_path(w.grid_hw, *(wl.bf16_bits(t[n]) for n in ("q", "k", "v")),
+                           wl.bf16_bits(t["norm_w"]), w.eps, w.theta, rows=rows)
+    assert_close(out[torch.from_numpy(rows).cuda()], ref, what=w.name)
+
+
+LENGTH_CASES = [
+    ([64, 60], 4, 32),
+    ([1], 2, 80),
+    ([0, 1, 0, 63, 64, 65, 127, 128, 129, 0], 3, 80),
+    ([300, 1, 257, 511, 512, 513], 2, 128),
+    ([5, 3000, 7], 2, 80),
+    ([7, 9, 2100], 2, 64),
+    ([200, 33, 96, 17], 4, 96),
+    ([1000], 1, 32),
+]
+
+
+@pytest.mark.parametrize("lengths,H,D", LENGTH_CASES)
+def test_attention_parity_lengths(lengths, H, D):
+    w = wl.from_lengths(lengths, H, D, max_seqlen_meta=131072)
+    t = w.tensors()
+    cu = torch.from_numpy(w.cu_seqlens).cuda()
+    q, k, v = (t[n].cuda() for n in ("q", "k", "v"))
+    status = vit.new_status()
+    out = vit.varlen_attn(q, k, v, cu, w.max_seqlen, status=status)
+    assert vit.read_status(status) == 0
+    ref = oracle.attention(*(oracle.widen(wl.bf16_bits(t[n])) for n in ("q", "k", "v")), w.cu_seqlens)
+    assert_close(out, ref, what=str(lengths))
+
+
+def test_attention_parity_explicit_scale():
+    w = wl.from_lengths([130, 70], 2, 80)
+    t = w.tensors()
+    q, k, v = (t[n].cuda() for n in ("q", "k", "v"))
+    out = vit.varlen_attn(q, k, v, torch.from_numpy(w.cu_seqlens).cuda(), w.max_seqlen, scale=0.05)
+    ref = oracle.attention(*(oracle.widen(wl.bf16_bits(t[n])) for n in ("q", "k", "v")), w.cu_seqlens, scale=0.05)
+    assert_close(out, ref, what="scale=0.05")

@@ -1,0 +1,204 @@
+"""GB300 (sm_103a) varlen ViT encoder attention: thin Python binding of libvitattn.
+
+Argument marshalling only: every step runs in the library's CUDA kernels,
+reached through its C ABI (include/vit_attn.h). PyTorch provides device
+memory and the current stream. There is no CPU or eager fallback: if the
+library is not built, every call raises.
+
+    inv_freq, pos_hw, cu = rope_freqs(grid_hw, T, head_dim)       # 2D RoPE table + positions
+    qk_norm_rope(q, k, pos_hw, inv_freq, norm_w, eps, inplace=True)
+    out = varlen_attn(q, k, v, cu, max_seqlen)                    # [T, H, D] bf16
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libvitattn.so")
+MAX_SEGMENTS = 8192
+HEAD_DIMS = (32, 64, 80, 96, 128)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class VitError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (status {code})")
+
+
+class _KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libvitattn (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                                   "g.build()'` (needs nvcc); there is no fallback implementation")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+            L.vit_version.restype = ctypes.c_char_p
+            L.vit_status_string.restype = ctypes.c_char_p
+            L.vit_status_string.argtypes = [i32]
+            L.vit_device_supported.argtypes = [i32]
+            L.vit_rope_freqs.argtypes = [i32, f32, vp, i32, i64, vp, vp, vp, vp, vp]
+            L.vit_qk_norm_rope.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i64, i64, vp, vp, vp, f32, vp]
+            L.vit_varlen_attn_workspace_size.restype = sz
+            L.vit_varlen_attn_workspace_size.argtypes = [i64, i32, i32, i32]
+            L.vit_varlen_attn.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, vp, i32, i32, f32, vp, i64, vp,
+                                          sz, vp, vp]
+            L.vit_read_status.argtypes = [vp, vp]
+            L.vit_launch_count.restype = i64
+            L.vit_kernel_timing.argtypes = [i32]
+            L.vit_kernel_timing_read.argtypes = [ctypes.POINTER(_KernelTime), i32]
+            for fn in ("vit_device_supported", "vit_rope_freqs", "vit_qk_norm_rope", "vit_varlen_attn",
+                       "vit_read_status", "vit_kernel_timing", "vit_kernel_timing_read"):
+                getattr(L, fn).restype = i32
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().vit_status_string(int(code)).decode()
+
+
+def version() -> str:
+    return lib().vit_version().decode()
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise VitError(code, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _tok_stride(t: torch.Tensor, name: str, H: int, D: int) -> int:
+    if t.dim() != 3 or t.shape[1] != H or t.shape[2] != D:
+        raise ValueError(f"{name} must be [T, {H}, {D}], got {tuple(t.shape)}")
+    if t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA bfloat16 tensor")
+    if t.stride(2) != 1 or t.stride(1) != D:
+        raise ValueError(f"{name} needs head stride D and unit element stride (got strides {t.stride()})")
+    return t.stride(0)
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word for the device-detected errors of the calls."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def read_status(status: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return the status word (0 = ok)."""
+    code = lib().vit_read_status(_ptr(status), _stream(stream))
+    return int(code)
+
+
+def rope_freqs(grid_hw: torch.Tensor, total_tokens: int, head_dim: int, theta: float = 10000.0, *,
+               status: torch.Tensor | None = None, stream=None):
+    """2D RoPE frequency table (dim = head_dim/2), per-token (row, col) and cu_seqlens from a device grid list."""
+    if grid_hw.dtype != torch.int32 or not grid_hw.is_cuda or not grid_hw.is_contiguous():
+        raise ValueError("grid_hw must be a contiguous CUDA int32 tensor [n_img, 2]")
+    n = grid_hw.numel() // 2
+    dev = grid_hw.device
+    dim = head_dim // 2
+    inv_freq = torch.empty(dim // 2, dtype=torch.float32, device=dev)
+    pos = torch.empty((total_tokens, 2), dtype=torch.int32, device=dev)
+    cu = torch.empty(n + 1, dtype=torch.int32, device=dev)
+    _check(lib().vit_rope_freqs(dim, float(theta), _ptr(grid_hw), n, int(total_tokens), _ptr(inv_freq), _ptr(pos),
+                                _ptr(cu), _ptr(status), _stream(stream)), "vit_rope_freqs")
+    return inv_freq, pos, cu
+
+
+def qk_norm_rope(q: torch.Tensor, k: torch.Tensor, pos_hw: torch.Tensor, inv_freq: torch.Tensor,
+                 norm_w: torch.Tensor | None = None, eps: float = 1e-6, *, q_out: torch.Tensor | None = None,
+                 k_out: torch.Tensor | None = None, inplace: bool = False, stream=None):
+    """QK-RMSNorm (if norm_w [2, D] is given) + 2D RoPE. Returns (q', k')."""
+    T, H, D = q.shape
+    qs = _tok_stride(q, "q", H, D)
+    ks = _tok_stride(k, "k", H, D)
+    if inplace:
+        q_out, k_out = q, k
+    if q_out is None:
+        q_out = torch.empty((T, H, D), dtype=q.dtype, device=q.device)
+    if k_out is None:
+        k_out = torch.empty((T, H, D), dtype=k.dtype, device=k.device)
+    qos = _tok_stride(q_out, "q_out", H, D)
+    kos = _tok_stride(k_out, "k_out", H, D)
+    if norm_w is not None and (norm_w.dtype != torch.bfloat16 or norm_w.numel() != 2 * D
+                               or not norm_w.is_contiguous()):
+        raise ValueError("norm_w must be a contiguous bfloat16 tensor [2, D]")
+    _check(lib().vit_qk_norm_rope(_ptr(q), _ptr(q_out), _ptr(k), _ptr(k_out), T, H, D, qs, qos, ks, kos,
+                                  _ptr(pos_hw), _ptr(inv_freq), _ptr(norm_w), float(eps), _stream(stream)),
+           "vit_qk_norm_rope")
+    return q_out, k_out
+
+
+def workspace_size(T: int, H: int, B: int, D: int) -> int:
+    return int(lib().vit_varlen_attn_workspace_size(int(T), int(H), int(B), int(D)))
+
+
+def varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor | None,
+                max_seqlen: int, scale: float | None = None, *, num_segments: int | None = None,
+                out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Non-causal attention inside each packed segment. q, k, v [T, H, D] bf16 -> out [T, H, D] bf16."""
+    T, H, D = q.shape
+    qs, ks, vs = _tok_stride(q, "q", H, D), _tok_stride(k, "k", H, D), _tok_stride(v, "v", H, D)
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or not cu_seqlens.is_contiguous():
+            raise ValueError("cu_seqlens must be a contiguous CUDA int32 tensor [B + 1]")
+        B = cu_seqlens.numel() - 1
+    else:
+        if num_segments is None:
+            raise ValueError("num_segments is required when cu_seqlens is None")
+        B = int(num_segments)
+    if out is None:
+        out = torch.empty((T, H, D), dtype=q.dtype, device=q.device)
+    os_ = _tok_stride(out, "out", H, D)
+    need = workspace_size(T, H, B, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().vit_varlen_attn(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, _ptr(cu_seqlens), B,
+                                 int(max_seqlen), float(scale) if scale is not None else 0.0, _ptr(out), os_,
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+                                 _stream(stream)), "vit_varlen_attn")
+    return out
+
+
+def launch_count() -> int:
+    return int(lib().vit_launch_count())
+
+
+def kernel_timing(enable: bool) -> bool:
+    return bool(lib().vit_kernel_timing(1 if enable else 0))
+
+
+def kernel_timing_read(max_entries: int = 32) -> dict:
+    """{kernel name: (launches, total ms)} for launches timed since the last read (synchronises)."""
+    arr = (_KernelTime * max_entries)()
+    n = lib().vit_kernel_timing_read(arr, max_entries)
+    if n < 0:
+        raise VitError(-8, "vit_kernel_timing_read")
+    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms)) for i in range(n)}
+
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)

@@ -1,0 +1,195 @@
+// C ABI of libvitattn: argument validation on the host, then kernel launches.
+// Every check that can be made without reading device memory is made here and
+// returns an error before anything is launched; device-side checks (segment
+// offsets, grid sums) are made by the kernels and reported through status_dev.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace vit {
+size_t schedule_smem_bytes(int B);
+int attn_short_bm();
+}  // namespace vit
+
+using namespace vit;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];         // 0 = not queried yet
+int g_supported[kMaxDevices];   // 0 = not queried, 1 = yes, -1 = no
+std::mutex g_dev_mutex;
+
+vit_status_t device_info(int *num_sms)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VIT_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return VIT_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_supported[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return VIT_ERR_CUDA;
+        g_supported[dev] = (major == 10 && minor == 3) ? 1 : -1;
+        g_sms[dev] = sms;
+    }
+    if (g_supported[dev] < 0) return VIT_ERR_UNSUPPORTED_DEVICE;
+    if (num_sms) *num_sms = g_sms[dev];
+    return VIT_OK;
+}
+
+bool head_dim_ok(int D) { return D == 32 || D == 64 || D == 80 || D == 96 || D == 128; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool stride_ok(int64_t s, int H, int D) { return s >= (int64_t)H * D && s % 8 == 0; }
+
+vit_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? VIT_OK : VIT_ERR_CUDA; }
+
+constexpr int64_t kMaxTokens = (int64_t)1 << 31;
+
+}  // namespace
+
+extern "C" {
+
+const char *vit_version(void) { return "vitattn 0.1 (sm_103a)"; }
+
+const char *vit_status_string(vit_status_t s)
+{
+    switch (s) {
+        case VIT_OK: return "ok";
+        case VIT_ERR_NULL_POINTER: return "a required pointer is NULL";
+        case VIT_ERR_BAD_HEAD_DIM: return "head_dim must be one of 32, 64, 80, 96, 128";
+        case VIT_ERR_BAD_SHAPE: return "invalid tensor shape (T, H, B)";
+        case VIT_ERR_BAD_STRIDE: return "token stride must be >= H*D and a multiple of 8 elements";
+        case VIT_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+        case VIT_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than vit_varlen_attn_workspace_size()";
+        case VIT_ERR_TOO_MANY_SEGMENTS: return "more segments than VIT_MAX_SEGMENTS";
+        case VIT_ERR_CUDA: return "a CUDA runtime call failed";
+        case VIT_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
+        case VIT_ERR_BAD_SEQLENS: return "cu_seqlens invalid: cu[0] != 0, decreasing, or cu[B] != T";
+        case VIT_ERR_SEQLEN_EXCEEDS_MAX: return "a segment is longer than max_seqlen";
+        case VIT_ERR_GRID_MISMATCH: return "patch grid does not sum to T (or has negative sides)";
+        case VIT_ERR_TIMEOUT: return "a bounded device-side wait expired";
+        case VIT_ERR_BAD_ARGUMENT: return "invalid argument";
+        default: return "unknown status";
+    }
+}
+
+vit_status_t vit_device_supported(int device)
+{
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess)
+        return VIT_ERR_CUDA;
+    return (major == 10 && minor == 3) ? VIT_OK : VIT_ERR_UNSUPPORTED_DEVICE;
+}
+
+vit_status_t vit_rope_freqs(int dim, float theta, const int32_t *grid_hw, int n_img, int64_t T, float *inv_freq,
+                            int32_t *pos_hw, int32_t *cu_seqlens, int32_t *status_dev, vit_stream_t stream)
+{
+    if (dim < 2 || dim % 2 != 0 || dim > 256) return VIT_ERR_BAD_ARGUMENT;
+    if (!(theta > 0.f) || !isfinite(theta)) return VIT_ERR_BAD_ARGUMENT;
+    if (n_img < 0 || T < 0 || T >= kMaxTokens) return VIT_ERR_BAD_SHAPE;
+    if (n_img > VIT_MAX_SEGMENTS) return VIT_ERR_TOO_MANY_SEGMENTS;
+    if (n_img > 0 && !grid_hw) return VIT_ERR_NULL_POINTER;
+    if (pos_hw && ((uintptr_t)pos_hw & 7u)) return VIT_ERR_MISALIGNED;
+    if (!inv_freq && !pos_hw && !cu_seqlens) return VIT_OK;
+    vit_status_t st = device_info(nullptr);
+    if (st != VIT_OK) return st;
+    return from_cuda(launch_rope_freqs(dim, theta, grid_hw, n_img, T, inv_freq, pos_hw, cu_seqlens, status_dev,
+                                       (cudaStream_t)stream));
+}
+
+vit_status_t vit_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T, int H, int D,
+                              int64_t q_in_stride, int64_t q_out_stride, int64_t k_in_stride, int64_t k_out_stride,
+                              const int32_t *pos_hw, const float *inv_freq, const void *norm_w, float eps,
+                              vit_stream_t stream)
+{
+    if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
+    if (T < 0 || T >= kMaxTokens || H < 1) return VIT_ERR_BAD_SHAPE;
+    if (!(eps >= 0.f) || !isfinite(eps)) return VIT_ERR_BAD_ARGUMENT;
+    if (T == 0) return VIT_OK;
+    if (!q_in || !q_out || !k_in || !k_out || !pos_hw || !inv_freq) return VIT_ERR_NULL_POINTER;
+    if (!stride_ok(q_in_stride, H, D) || !stride_ok(q_out_stride, H, D) || !stride_ok(k_in_stride, H, D) ||
+        !stride_ok(k_out_stride, H, D))
+        return VIT_ERR_BAD_STRIDE;
+    if ((q_in == q_out && q_in_stride != q_out_stride) || (k_in == k_out && k_in_stride != k_out_stride))
+        return VIT_ERR_BAD_STRIDE;
+    if (!aligned16(q_in) || !aligned16(q_out) || !aligned16(k_in) || !aligned16(k_out) ||
+        ((uintptr_t)pos_hw & 7u) || ((uintptr_t)inv_freq & 3u) || ((uintptr_t)norm_w & 1u))
+        return VIT_ERR_MISALIGNED;
+    int sms = 0;
+    vit_status_t st = device_info(&sms);
+    if (st != VIT_OK) return st;
+    return from_cuda(launch_qk_norm_rope(q_in, q_out, k_in, k_out, T, H, D, q_in_stride, q_out_stride, k_in_stride,
+                                         k_out_stride, pos_hw, inv_freq, norm_w, eps, sms, (cudaStream_t)stream));
+}
+
+size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D)
+{
+    if (T < 0 || T >= kMaxTokens || H < 1 || B < 0 || B > VIT_MAX_SEGMENTS || !head_dim_ok(D)) return 0;
+    const int64_t items = max_items(T, H, B, attn_short_bm());
+    return sizeof(WsHeader) + sizeof(Item) * (size_t)items;
+}
+
+vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_t T, int H, int D, int64_t q_stride,
+                             int64_t k_stride, int64_t v_stride, const int32_t *cu_seqlens, int B, int max_seqlen,
+                             float scale, void *out, int64_t out_stride, void *workspace, size_t workspace_bytes,
+                             int32_t *status_dev, vit_stream_t stream)
+{
+    if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
+    if (T < 0 || T >= kMaxTokens || H < 1 || B < 0) return VIT_ERR_BAD_SHAPE;
+    if (B > VIT_MAX_SEGMENTS) return VIT_ERR_TOO_MANY_SEGMENTS;
+    if (B == 0) return T == 0 ? VIT_OK : VIT_ERR_BAD_SHAPE;
+    if (max_seqlen < 0 || (T > 0 && max_seqlen < 1)) return VIT_ERR_BAD_ARGUMENT;
+    if (isnan(scale) || isinf(scale)) return VIT_ERR_BAD_ARGUMENT;
+    if (!cu_seqlens && T % B != 0) return VIT_ERR_BAD_ARGUMENT;
+    if (T > 0) {
+        if (!q || !k || !v || !out) return VIT_ERR_NULL_POINTER;
+        if (!stride_ok(q_stride, H, D) || !stride_ok(k_stride, H, D) || !stride_ok(v_stride, H, D) ||
+            !stride_ok(out_stride, H, D))
+            return VIT_ERR_BAD_STRIDE;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return VIT_ERR_MISALIGNED;
+    }
+    if (!workspace) return VIT_ERR_NULL_POINTER;
+    if (!aligned16(workspace) || ((uintptr_t)cu_seqlens & 3u)) return VIT_ERR_MISALIGNED;
+    const size_t need = vit_varlen_attn_workspace_size(T, H, B, D);
+    if (need == 0) return VIT_ERR_BAD_SHAPE;
+    if (workspace_bytes < need) return VIT_ERR_WORKSPACE_TOO_SMALL;
+
+    int sms = 0;
+    vit_status_t st = device_info(&sms);
+    if (st != VIT_OK) return st;
+    if (scale <= 0.f) scale = 1.0f / sqrtf((float)D);
+    const float scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t s = (cudaStream_t)stream;
+
+    WsHeader *hdr = static_cast<WsHeader *>(workspace);
+    Item *items = reinterpret_cast<Item *>(hdr + 1);
+    SchedParams sp;
+    sp.short_max = 0x7fffffff;                       // every segment on the short-segment kernel
+    sp.bm_long = 256;
+    sp.bm_short = attn_short_bm();
+    cudaError_t e = launch_schedule(cu_seqlens, B, T, H, max_seqlen, sp, hdr, items, status_dev, s);
+    if (e != cudaSuccess) return VIT_ERR_CUDA;
+    if (T == 0) return VIT_OK;
+    e = launch_attn_short(q, k, v, q_stride, k_stride, v_stride, out, out_stride, D, scale_log2, hdr, items,
+                          max_items(T, H, B, sp.bm_short), sms, s);
+    return from_cuda(e);
+}
+
+vit_status_t vit_read_status(const int32_t *status_dev, vit_stream_t stream)
+{
+    if (!status_dev) return VIT_ERR_NULL_POINTER;
+    int32_t h = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(&h, status_dev, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess) return VIT_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return VIT_ERR_CUDA;
+    return h;
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// Internal declarations shared by the CUDA translation units of libvitattn.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "vit_attn.h"
+
+namespace vit {
+
+// Work item of the attention kernels: one (segment, head, q-block).
+//   x = first token of the segment, y = segment length,
+//   z = first query token of the block, w = head.
+using Item = int4;
+
+// Header at the start of the attention workspace, written by the scheduler.
+struct WsHeader {
+    int32_t n_long;      // items [0, n_long) go to the long-segment kernel
+    int32_t n_short;     // items [n_long, n_long + n_short) go to the short-segment kernel
+    int32_t bm_long;     // query rows per long item
+    int32_t bm_short;    // query rows per short item
+    int32_t error;       // device-detected error of the last scheduling pass (0 = none)
+    int32_t pad[11];
+};
+static_assert(sizeof(WsHeader) == 64, "header is 64 bytes");
+
+// Scheduling parameters chosen by the host.
+struct SchedParams {
+    int short_max;   // segments with length <= short_max use the short-segment kernel
+    int bm_long;     // q rows per long item
+    int bm_short;    // q rows per short item
+};
+
+// Upper bound on the number of items of one class for these sizes.
+inline int64_t max_items(int64_t T, int H, int B, int bm) {
+    return (int64_t)H * ((T + bm - 1) / bm + B);
+}
+
+// Record a device-side error (first error wins; never overwrites a stored code).
+__device__ __forceinline__ void report_error(int32_t *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ---- launch bookkeeping (instrument.cpp) ----
+struct LaunchScope {
+    LaunchScope(const char *name, cudaStream_t stream);
+    ~LaunchScope();
+    const char *name_;
+    cudaStream_t stream_;
+    void *slot_;
+};
+
+// ---- launchers (one per translation unit) ----
+cudaError_t launch_rope_freqs(int dim, float theta, const int32_t *grid_hw, int n_img, int64_t T,
+                              float *inv_freq, int32_t *pos_hw, int32_t *cu_seqlens, int32_t *status,
+                              cudaStream_t stream);
+
+cudaError_t launch_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T,
+                                int H, int D, int64_t q_in_stride, int64_t q_out_stride,
+                                int64_t k_in_stride, int64_t k_out_stride, const int32_t *pos_hw,
+                                const float *inv_freq, const void *norm_w, float eps, int num_sms,
+                                cudaStream_t stream);
+
+cudaError_t launch_schedule(const int32_t *cu_seqlens, int B, int64_t T, int H, int max_seqlen,
+                            SchedParams sp, WsHeader *hdr, Item *items, int32_t *status,
+                            cudaStream_t stream);
+
+cudaError_t launch_attn_short(const void *q, const void *k, const void *v, int64_t q_stride,
+                              int64_t k_stride, int64_t v_stride, void *out, int64_t out_stride,
+                              int D, float scale_log2, const WsHeader *hdr, const Item *items,
+                              int64_t max_items_short, int num_sms, cudaStream_t stream);
+
+}  // namespace vit

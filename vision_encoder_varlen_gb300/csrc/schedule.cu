@@ -1,0 +1,188 @@
+// Segment-aware work scheduler for the varlen attention kernels.
+//
+// From cu_seqlens alone, on the device (no host sync, so a caller can stay
+// inside a CUDA graph: tokenspeed mm_encoder_attention.py, _varlen_metadata,
+// keeps max_seqlen off the GPU->CPU path for the same reason), one block:
+//   1. validates the offsets (cu[0] == 0, non-decreasing, cu[B] == T, every
+//      length <= max_seqlen; max_seqlen may be a padded bucket bound,
+//      round_up_to_bucket on the same page);
+//   2. orders segments longest first (LPT) with a bitonic sort of
+//      (length desc, index asc) keys, so the order is deterministic;
+//   3. expands every segment into (segment, head, q-block) work items: long
+//      segments into blocks of bm_long query rows for the long-segment kernel,
+//      short ones into blocks of bm_short rows for the short-segment kernel.
+//      Items never straddle two segments; the q-block is the fastest index,
+//      so concurrently running CTAs share one head's K/V in L2.
+// On invalid offsets it records the error and publishes zero items, so the
+// attention kernels that follow compute nothing.
+#include "internal.h"
+
+namespace vit {
+namespace {
+
+constexpr int kThreads = 1024;
+
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t *s_warp, int64_t *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = s_warp[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        s_warp[lane] = w;                // inclusive over warps
+    }
+    __syncthreads();
+    const int64_t before = (warp > 0 ? s_warp[warp - 1] : 0) + x - v;
+    *total = s_warp[31];
+    __syncthreads();
+    return before;
+}
+
+__global__ void __launch_bounds__(kThreads)
+schedule_kernel(const int32_t *__restrict__ cu_seqlens, int B, int64_t T, int H, int max_seqlen,
+                SchedParams sp, WsHeader *hdr, Item *items, int32_t *status)
+{
+    extern __shared__ unsigned long long s_key[];      // [NP] sort keys, then [B] int32 offsets reuse
+    __shared__ int64_t s_warp[32];
+    __shared__ int s_err;
+    const int tid = threadIdx.x;
+    int NP = 1;
+    while (NP < B) NP <<= 1;
+    int32_t *s_start = reinterpret_cast<int32_t *>(s_key + NP);   // [B] segment start by segment index
+    int32_t *s_len = s_start + B;                                  // [B] segment length by segment index
+    int32_t *s_off = s_len + B;                                    // [B] first item of sorted position p
+
+    if (tid == 0) s_err = 0;
+    __syncthreads();
+
+    // ---- 1. offsets and validation
+    const int64_t uni = B > 0 ? T / B : 0;
+    for (int i = tid; i < B; i += kThreads) {
+        int64_t a, b;
+        if (cu_seqlens) {
+            a = cu_seqlens[i];
+            b = cu_seqlens[i + 1];
+        } else {
+            a = uni * i;
+            b = uni * (i + 1);
+        }
+        if (i == 0 && a != 0) atomicMax(&s_err, 1);
+        if (i == B - 1 && b != T) atomicMax(&s_err, 1);
+        if (b < a) atomicMax(&s_err, 1);
+        else if (b - a > (int64_t)max_seqlen) atomicMax(&s_err, 2);
+        s_start[i] = (int32_t)a;
+        s_len[i] = (int32_t)(b > a ? b - a : 0);
+    }
+    __syncthreads();
+    if (s_err) {
+        if (tid == 0) {
+            hdr->n_long = 0;
+            hdr->n_short = 0;
+            hdr->error = s_err == 1 ? VIT_ERR_BAD_SEQLENS : VIT_ERR_SEQLEN_EXCEEDS_MAX;
+            report_error(status, hdr->error);
+        }
+        return;
+    }
+
+    // ---- 2. LPT order: ascending keys = descending length, then ascending index
+    for (int i = tid; i < NP; i += kThreads)
+        s_key[i] = i < B ? ((unsigned long long)(0x7fffffffu - (uint32_t)s_len[i]) << 32) | (uint32_t)i
+                         : ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= NP; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < NP; i += kThreads) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const unsigned long long a = s_key[i], b = s_key[l];
+                    const bool up = (i & k) == 0;
+                    if ((a > b) == up) {
+                        s_key[i] = b;
+                        s_key[l] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+
+    // ---- 3. item counts per sorted position, exclusive scan, expansion
+    const int per = (B + kThreads - 1) / kThreads;
+    const int lo = min(tid * per, B), hi = min(lo + per, B);
+    int64_t local = 0, local_long = 0;
+    for (int p = lo; p < hi; ++p) {
+        const int seg = (int)(s_key[p] & 0xffffffffu);
+        const int len = s_len[seg];
+        const bool is_long = len > sp.short_max;
+        const int bm = is_long ? sp.bm_long : sp.bm_short;
+        const int64_t n = (int64_t)H * ((len + bm - 1) / bm);
+        local += n;
+        if (is_long) local_long += n;
+    }
+    int64_t total, total_long;
+    int64_t run = block_exclusive_scan(local, s_warp, &total);
+    block_exclusive_scan(local_long, s_warp, &total_long);
+    for (int p = lo; p < hi; ++p) {
+        const int seg = (int)(s_key[p] & 0xffffffffu);
+        const int len = s_len[seg];
+        const int bm = len > sp.short_max ? sp.bm_long : sp.bm_short;
+        s_off[p] = (int32_t)run;
+        run += (int64_t)H * ((len + bm - 1) / bm);
+    }
+    __syncthreads();
+    for (int p = 0; p < B; ++p) {
+        const int seg = (int)(s_key[p] & 0xffffffffu);
+        const int len = s_len[seg];
+        if (len == 0) continue;
+        const int bm = len > sp.short_max ? sp.bm_long : sp.bm_short;
+        const int nq = (len + bm - 1) / bm;
+        const int start = s_start[seg];
+        Item *dst = items + s_off[p];
+        for (int i = tid; i < H * nq; i += kThreads) {
+            const int h = i / nq, qb = i - h * nq;
+            dst[i] = make_int4(start, len, start + qb * bm, h);
+        }
+    }
+    if (tid == 0) {
+        hdr->n_long = (int32_t)total_long;
+        hdr->n_short = (int32_t)(total - total_long);
+        hdr->bm_long = sp.bm_long;
+        hdr->bm_short = sp.bm_short;
+        hdr->error = 0;
+    }
+}
+
+}  // namespace
+
+size_t schedule_smem_bytes(int B)
+{
+    int NP = 1;
+    while (NP < B) NP <<= 1;
+    return sizeof(unsigned long long) * (size_t)NP + sizeof(int32_t) * 3 * (size_t)B;
+}
+
+cudaError_t launch_schedule(const int32_t *cu_seqlens, int B, int64_t T, int H, int max_seqlen,
+                            SchedParams sp, WsHeader *hdr, Item *items, int32_t *status, cudaStream_t stream)
+{
+    const size_t smem = schedule_smem_bytes(B);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    LaunchScope scope("schedule", stream);
+    schedule_kernel<<<1, kThreads, smem, stream>>>(cu_seqlens, B, T, H, max_seqlen, sp, hdr, items, status);
+    return cudaGetLastError();
+}
+
+}  // namespace vit
