@@ -172,6 +172,16 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
                              int32_t *status_dev, vit_stream_t stream);
 
 /*
+ * Kernel split of vit_varlen_attn: segments longer than `short_max` tokens run
+ * on the tcgen05/TMEM long-segment kernel (256 query rows per work item), the
+ * others on the short-segment kernel (64 query rows per item). Default 128.
+ * 0 sends every segment to the long kernel, INT_MAX every segment to the short
+ * one; the results agree within the output tolerance either way. Process-wide
+ * setting read at each call; returns the previous value.
+ */
+int vit_set_short_segment_max(int short_max);
+
+/*
  * Synchronise `stream`, then read the status word. Returns VIT_OK, the first
  * device-detected error code stored there, or VIT_ERR_CUDA when the stream or
  * the copy failed. The only call of the compute path that blocks the host.

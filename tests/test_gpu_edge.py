@@ -20,6 +20,16 @@ def _built():
     _build.build()
 
 
+SPLITS = {"default": 128, "all_long": 0, "all_short": 2 ** 31 - 1}
+
+
+@pytest.fixture(params=list(SPLITS))
+def split(request):
+    prev = vit.set_short_segment_max(SPLITS[request.param])
+    yield request.param
+    vit.set_short_segment_max(prev)
+
+
 def _inputs(lengths, H, D, seed=0):
     w = wl.from_lengths(lengths, H, D, seed=wl.SEED_BASE + seed, max_seqlen_meta=131072)
     t = w.tensors()
@@ -27,7 +37,7 @@ def _inputs(lengths, H, D, seed=0):
 
 
 @pytest.mark.parametrize("D", [80, 128])
-def test_segment_isolation_bitwise(D):
+def test_segment_isolation_bitwise(D, split):
     lengths = [130, 1, 700, 64, 255]
     w, t, cu, (q, k, v) = _inputs(lengths, 2, D)
     base = vit.varlen_attn(q, k, v, cu, w.max_seqlen).clone()
@@ -45,7 +55,7 @@ def test_segment_isolation_bitwise(D):
         assert not torch.equal(pert[a:b], base[a:b])
 
 
-def test_deterministic_bitwise():
+def test_deterministic_bitwise(split):
     w, t, cu, (q, k, v) = _inputs([3000, 17, 900], 4, 80, seed=3)
     ws = torch.empty(vit.workspace_size(w.total_tokens, 4, 3, 80), dtype=torch.uint8, device="cuda")
     a = vit.varlen_attn(q, k, v, cu, w.max_seqlen, workspace=ws).clone()
@@ -54,7 +64,7 @@ def test_deterministic_bitwise():
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def test_strided_packed_qkv_and_strided_out():
+def test_strided_packed_qkv_and_strided_out(split):
     lengths = [100, 300]
     H, D = 3, 80
     w, t, cu, _ = _inputs(lengths, H, D, seed=4)
@@ -70,7 +80,7 @@ def test_strided_packed_qkv_and_strided_out():
     assert torch.all(big[:, 0] == 7.0) and torch.all(big[:, H + 1] == 7.0)
 
 
-def test_uniform_segments_without_cu_seqlens():
+def test_uniform_segments_without_cu_seqlens(split):
     H, D, B, L = 2, 64, 4, 96
     w, t, cu, (q, k, v) = _inputs([L] * B, H, D, seed=5)
     out = vit.varlen_attn(q, k, v, None, L, num_segments=B)
@@ -97,7 +107,7 @@ def test_in_place_prologue_matches_out_of_place():
     ([0, 10, 19], 100, -10),         # does not end at T
     ([0, 10, 20], 9, -11),           # a segment longer than max_seqlen
 ])
-def test_device_detected_bad_seqlens_leave_output_untouched(cu_list, max_seqlen, code):
+def test_device_detected_bad_seqlens_leave_output_untouched(cu_list, max_seqlen, code, split):
     T, H, D = 20, 2, 80
     g = torch.Generator().manual_seed(0)
     q, k, v = (torch.randn(T, H, D, generator=g).to(torch.bfloat16).cuda() for _ in range(3))

@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
             L.vit_varlen_attn.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, vp, i32, i32, f32, vp, i64, vp,
                                           sz, vp, vp]
             L.vit_read_status.argtypes = [vp, vp]
+            L.vit_set_short_segment_max.argtypes = [i32]
+            L.vit_set_short_segment_max.restype = i32
             L.vit_launch_count.restype = i64
             L.vit_kernel_timing.argtypes = [i32]
             L.vit_kernel_timing_read.argtypes = [ctypes.POINTER(_KernelTime), i32]
@@ -181,6 +183,12 @@ def varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: t
                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
                                  _stream(stream)), "vit_varlen_attn")
     return out
+
+
+def set_short_segment_max(short_max: int) -> int:
+    """Segments longer than short_max go to the tcgen05 long-segment kernel (default 128).
+    Returns the previous value."""
+    return int(lib().vit_set_short_segment_max(int(short_max)))
 
 
 def launch_count() -> int:

@@ -5,6 +5,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -12,6 +13,7 @@
 namespace vit {
 size_t schedule_smem_bytes(int B);
 int attn_short_bm();
+int attn_long_bm();
 }  // namespace vit
 
 using namespace vit;
@@ -50,6 +52,9 @@ bool stride_ok(int64_t s, int H, int D) { return s >= (int64_t)H * D && s % 8 ==
 vit_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? VIT_OK : VIT_ERR_CUDA; }
 
 constexpr int64_t kMaxTokens = (int64_t)1 << 31;
+
+// Segments longer than this run on the tcgen05 long-segment kernel.
+std::atomic<int> g_short_max{128};
 
 }  // namespace
 
@@ -171,15 +176,29 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
     WsHeader *hdr = static_cast<WsHeader *>(workspace);
     Item *items = reinterpret_cast<Item *>(hdr + 1);
     SchedParams sp;
-    sp.short_max = 0x7fffffff;                       // every segment on the short-segment kernel
-    sp.bm_long = 256;
+    sp.short_max = g_short_max.load();
+    sp.bm_long = attn_long_bm();
     sp.bm_short = attn_short_bm();
     cudaError_t e = launch_schedule(cu_seqlens, B, T, H, max_seqlen, sp, hdr, items, status_dev, s);
     if (e != cudaSuccess) return VIT_ERR_CUDA;
     if (T == 0) return VIT_OK;
-    e = launch_attn_short(q, k, v, q_stride, k_stride, v_stride, out, out_stride, D, scale_log2, hdr, items,
-                          max_items(T, H, B, sp.bm_short), sms, s);
+    // a segment can only be long when the bound allows it
+    const int64_t longest = cu_seqlens ? (int64_t)max_seqlen : T / B;
+    if (longest > sp.short_max) {
+        e = launch_attn_long(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, D, scale_log2, hdr, items,
+                             max_items(T, H, B, sp.bm_long), sms, status_dev, s);
+        if (e != cudaSuccess) return VIT_ERR_CUDA;
+    }
+    if (sp.short_max > 0) {
+        e = launch_attn_short(q, k, v, q_stride, k_stride, v_stride, out, out_stride, D, scale_log2, hdr, items,
+                              max_items(T, H, B, sp.bm_short), sms, s);
+    }
     return from_cuda(e);
+}
+
+int vit_set_short_segment_max(int short_max)
+{
+    return g_short_max.exchange(short_max < 0 ? 0 : short_max);
 }
 
 vit_status_t vit_read_status(const int32_t *status_dev, vit_stream_t stream)

@@ -1,0 +1,463 @@
+// Long-segment varlen attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Same result as the short-segment kernel: for each (segment, head) the plain
+// softmax(scale * q k^T) v over that segment's keys only (vLLM Dots
+// vision_attention page, VisionAttentionV2.forward / VisionAttention.forward
+// with its block-diagonal mask), softmax in fp32, P rounded to bf16 for the
+// P.V product, fp32 accumulation in TMEM, bf16 output.
+//
+// One work item = (segment, head, 256 query rows) = two 128-row Q tiles that
+// share every K/V tile the TMA warp streams in. Persistent CTAs (one per SM)
+// walk the scheduler's longest-first list. Warp roles (320 threads):
+//   warp 0      TMA producer: Q tiles per item, K and V tiles into a ring of
+//               STAGES slots; 16-column (32-byte) slabs with 32-byte swizzle,
+//               so any head_dim that is a multiple of 16 maps exactly.
+//   warp 1      TMEM owner and single-thread MMA issuer:
+//                 S_i = Q_i K^T     (SS MMA, M=128, N=BN, K=D)   into TMEM
+//                 O_i += P V        (TS MMA, A=P from TMEM, B=V MN-major)
+//               issued in the order QK0(j+1), PV0(j), QK1(j+1), PV1(j) so the
+//               tensor pipe always has the other tile's work queued while a
+//               softmax group turns S into P.
+//   warps 2-5   softmax group 0 (tile 0), one TMEM lane = one query row per
+//   warps 6-9   softmax group 1 (tile 1)  thread: row max, lazy rescaling of
+//               O (only when the max grows by more than 2^8), exp2 with the
+//               scale folded in, row sum, P -> bf16 into a P region of TMEM
+//               shared by both tiles, and the epilogue O / l -> bf16 -> HBM.
+// TMEM (512 columns): S0 | S1 | O0 | O1 | P.  Keys past the segment end are
+// masked to -inf (they contribute exactly 0), query rows past it are never
+// stored, rows past T are zero-filled by TMA: no item reads or writes any
+// other segment's results. Every wait is bounded; a wait that expires sets
+// VIT_ERR_TIMEOUT, and all roles drain and free TMEM before exiting.
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace vit {
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreads = 320;
+constexpr int BM = 128;                       // rows per Q tile; two tiles per item
+constexpr long long kWaitBudget = 4000000000ll;   // clock cycles before a wait gives up (~2 s)
+
+template <int D> struct LongCfg {
+    static constexpr int BN = (D <= 96) ? 128 : 96;       // keys per tile
+    static constexpr int STAGES = 3;
+    static constexpr int NSLAB = D / 16;
+    static constexpr int Q_SLAB = BM * 32;                 // bytes of one 16-column slab of a Q tile
+    static constexpr int KV_SLAB = BN * 32;
+    static constexpr int Q_TILE = NSLAB * Q_SLAB;
+    static constexpr int KV_TILE = NSLAB * KV_SLAB;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
+    static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
+    static constexpr int DATA = OFF_V + STAGES * KV_TILE;
+    // > half of the SM's shared memory: exactly one CTA (one TMEM owner) per SM
+    static constexpr int SMEM = (DATA + 1024 > 118 * 1024) ? DATA + 1024 : 118 * 1024;
+    // TMEM columns
+    static constexpr int TS0 = 0, TS1 = BN, TO0 = 2 * BN, TO1 = 2 * BN + D, TP = 2 * BN + 2 * D;
+    static_assert(TP + BN / 2 <= 512, "TMEM budget");
+    static_assert(D % 16 == 0 && BN % 32 == 0, "tile shapes");
+};
+
+struct Bars {
+    uint64_t q_full, q_empty;
+    uint64_t k_full[3], v_full[3], kv_empty[3];
+    uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
+    uint64_t drain;
+};
+
+__device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_addr(&b); }
+
+template <int D>
+__global__ void __maxnreg__(200)
+attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out, int64_t out_stride,
+                 float scale_log2, const WsHeader *__restrict__ hdr, const Item *__restrict__ items,
+                 int32_t *status)
+{
+    using C = LongCfg<D>;
+    constexpr int BN = C::BN, ST = C::STAGES, NSLAB = C::NSLAB;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ Bars bars;
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_items = hdr->n_long;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        mbar_init(bar_addr(bars.q_full), 1);
+        mbar_init(bar_addr(bars.q_empty), 1);
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(bar_addr(bars.k_full[s]), 1);
+            mbar_init(bar_addr(bars.v_full[s]), 1);
+            mbar_init(bar_addr(bars.kv_empty[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_addr(bars.s_full[i]), 1);
+            mbar_init(bar_addr(bars.s_free[i]), 4);
+            mbar_init(bar_addr(bars.p_full[i]), 4);
+            mbar_init(bar_addr(bars.pv_done[i]), 1);
+            mbar_init(bar_addr(bars.o_free[i]), 4);
+        }
+        mbar_init(bar_addr(bars.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&s_tmem), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    auto fail = [&]() {
+        if (!s_abort) {
+            s_abort = 1;
+            report_error(status, VIT_ERR_TIMEOUT);
+        }
+    };
+    auto wait = [&](const uint64_t &b, uint32_t parity) -> bool {
+        if (mbar_wait(bar_addr(b), parity, (const volatile int *)&s_abort, kWaitBudget)) return true;
+        fail();
+        return false;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            uint32_t g = 0, q_it = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++q_it) {
+                const Item item = items[it];
+                const int seg0 = item.x, seg_len = item.y, q0 = item.z, head = item.w;
+                const int n_kv = (seg_len + BN - 1) / BN;
+                if (q_it > 0 && !(ok = wait(bars.q_empty, (q_it - 1) & 1))) break;
+                mbar_arrive_expect_tx(bar_addr(bars.q_full), 2 * C::Q_TILE);
+                for (int i = 0; i < 2; ++i)
+                    for (int s = 0; s < NSLAB; ++s)
+                        tma_load_2d(smem_addr(base + C::OFF_Q + i * C::Q_TILE + s * C::Q_SLAB), &tm_q,
+                                    head * D + 16 * s, q0 + BM * i, bar_addr(bars.q_full));
+                for (int j = 0; j < n_kv; ++j, ++g) {
+                    const int st = g % ST;
+                    if (g >= (uint32_t)ST && !(ok = wait(bars.kv_empty[st], (g / ST - 1) & 1))) break;
+                    const int row = seg0 + j * BN;
+                    mbar_arrive_expect_tx(bar_addr(bars.k_full[st]), C::KV_TILE);
+                    for (int s = 0; s < NSLAB; ++s)
+                        tma_load_2d(smem_addr(base + C::OFF_K + st * C::KV_TILE + s * C::KV_SLAB), &tm_k,
+                                    head * D + 16 * s, row, bar_addr(bars.k_full[st]));
+                    mbar_arrive_expect_tx(bar_addr(bars.v_full[st]), C::KV_TILE);
+                    for (int s = 0; s < NSLAB; ++s)
+                        tma_load_2d(smem_addr(base + C::OFF_V + st * C::KV_TILE + s * C::KV_SLAB), &tm_v,
+                                    head * D + 16 * s, row, bar_addr(bars.v_full[st]));
+                }
+            }
+            if (!ok) {
+                // let copies already issued land before the CTA's shared memory goes away
+                for (int s = 0; s < ST; ++s) {
+                    mbar_wait(bar_addr(bars.k_full[s]), 0, (const volatile int *)&s_abort, 0);
+                }
+                const long long t0 = clock64();
+                while (clock64() - t0 < 2000000) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t ID_QK = idesc_bf16(128, BN, 0, 0);
+            constexpr uint32_t ID_PV = idesc_bf16(128, D, 0, 1);
+            const uint32_t tS[2] = {tmem + C::TS0, tmem + C::TS1};
+            const uint32_t tO[2] = {tmem + C::TO0, tmem + C::TO1};
+            const uint32_t tP = tmem + C::TP;
+            const uint32_t q_base = smem_addr(base + C::OFF_Q);
+            const uint32_t k_base = smem_addr(base + C::OFF_K);
+            const uint32_t v_base = smem_addr(base + C::OFF_V);
+            uint32_t g = 0, item_cnt = 0;
+            uint32_t s_cnt[2] = {0, 0}, pv_cnt[2] = {0, 0};
+            bool ok = true;
+
+            auto issue_qk = [&](int i, int st) {
+                const uint32_t qa = q_base + i * C::Q_TILE, ka = k_base + st * C::KV_TILE;
+#pragma unroll
+                for (int kk = 0; kk < NSLAB; ++kk)
+                    mma_ss(tS[i], smem_desc(qa + kk * C::Q_SLAB, 16, 256, 6), smem_desc(ka + kk * C::KV_SLAB, 16, 256, 6),
+                           ID_QK, kk > 0);
+                mma_commit(bar_addr(bars.s_full[i]));
+                ++s_cnt[i];
+            };
+            auto issue_pv = [&](int i, int st, bool acc) {
+                const uint32_t va = v_base + st * C::KV_TILE;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tO[i], tP + kk * 8, smem_desc(va + kk * 16 * 32, C::KV_SLAB, 256, 6), ID_PV,
+                           (acc || kk > 0) ? 1u : 0u);
+                mma_commit(bar_addr(bars.pv_done[i]));
+                ++pv_cnt[i];
+            };
+
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_cnt) {
+                const Item item = items[it];
+                const int n_kv = (item.y + BN - 1) / BN;
+                if (!(ok = wait(bars.q_full, item_cnt & 1))) break;
+                // prologue: S0(0), S1(0)
+                if (!(ok = wait(bars.k_full[g % ST], (g / ST) & 1))) break;
+                for (int i = 0; i < 2 && ok; ++i) {
+                    if (s_cnt[i] > 0 && !(ok = wait(bars.s_free[i], (s_cnt[i] - 1) & 1))) break;
+                    tc_fence_after();
+                    issue_qk(i, g % ST);
+                }
+                if (!ok) break;
+                if (n_kv == 1) mma_commit(bar_addr(bars.q_empty));
+                for (int j = 0; j < n_kv && ok; ++j) {
+                    const uint32_t gj = g + j, st = gj % ST, st1 = (gj + 1) % ST;
+                    if (j + 1 < n_kv) {
+                        if (!(ok = wait(bars.k_full[st1], ((gj + 1) / ST) & 1))) break;
+                        if (!(ok = wait(bars.s_free[0], (s_cnt[0] - 1) & 1))) break;
+                        tc_fence_after();
+                        issue_qk(0, st1);
+                    }
+                    if (!(ok = wait(bars.v_full[st], (gj / ST) & 1))) break;
+                    if (j == 0 && item_cnt > 0 && !(ok = wait(bars.o_free[0], (item_cnt - 1) & 1))) break;
+                    if (!(ok = wait(bars.p_full[0], pv_cnt[0] & 1))) break;
+                    tc_fence_after();
+                    issue_pv(0, st, j > 0);
+                    if (j + 1 < n_kv) {
+                        if (!(ok = wait(bars.s_free[1], (s_cnt[1] - 1) & 1))) break;
+                        tc_fence_after();
+                        issue_qk(1, st1);
+                        if (j + 2 == n_kv) mma_commit(bar_addr(bars.q_empty));
+                    }
+                    if (j == 0 && item_cnt > 0 && !(ok = wait(bars.o_free[1], (item_cnt - 1) & 1))) break;
+                    if (!(ok = wait(bars.p_full[1], pv_cnt[1] & 1))) break;
+                    tc_fence_after();
+                    issue_pv(1, st, j > 0);
+                    mma_commit(bar_addr(bars.kv_empty[st]));
+                }
+                g += n_kv;
+            }
+            // drain: nothing of ours may still be running when TMEM is freed
+            mma_commit(bar_addr(bars.drain));
+            mbar_wait(bar_addr(bars.drain), 0, (const volatile int *)&s_abort, ok ? kWaitBudget : 200000000ll);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax groups
+        const int grp = (warp - 2) >> 2;                       // 0 or 1: which Q tile
+        const int quarter = warp & 3;                          // TMEM lane quarter this warp may access
+        const int row = quarter * 32 + lane;                   // row of the tile = TMEM lane
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t tS = t_lane + (grp ? C::TS1 : C::TS0);
+        const uint32_t tO = t_lane + (grp ? C::TO1 : C::TO0);
+        const uint32_t tP = t_lane + C::TP;
+        uint32_t s_cnt = 0, p_cnt = 0, item_cnt = 0;
+        bool ok = true;
+
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_cnt) {
+            const Item item = items[it];
+            const int seg0 = item.x, seg_len = item.y, q0 = item.z, head = item.w;
+            const int n_kv = (seg_len + BN - 1) / BN;
+            float m_run = -INFINITY, l_run = 0.f;
+
+            for (int j = 0; j < n_kv && ok; ++j) {
+                if (!(ok = wait(bars.s_full[grp], s_cnt & 1))) break;
+                tc_fence_after();
+                float s[BN];
+#pragma unroll
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + c, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[c + e] = __uint_as_float(r[e]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_addr(bars.s_free[grp]));
+                ++s_cnt;
+
+                const int kv_valid = seg_len - j * BN;         // keys of this tile inside the segment
+                if (kv_valid < BN) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c)
+                        if (c >= kv_valid) s[c] = -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+                const float m_tile = mx * scale_log2;
+                float alpha = 1.f;
+                if (m_tile > m_run + 8.f) {                    // lazy rescale: only when the max grows by > 2^8
+                    alpha = ex2(m_run - m_tile);
+                    m_run = m_tile;
+                }
+                const bool rescale = (j > 0) && (alpha != 1.f);
+                uint32_t pk[BN / 2];
+                float sum = 0.f;
+#pragma unroll
+                for (int c = 0; c < BN; c += 2) {
+                    const float p0 = ex2(fmaf(s[c], scale_log2, -m_run));
+                    const float p1 = ex2(fmaf(s[c + 1], scale_log2, -m_run));
+                    sum += p0 + p1;
+                    pk[c / 2] = pack_bf16x2(p0, p1);
+                }
+                l_run = l_run * alpha + sum;
+
+                // the shared P region is free once the previous P.V product finished; that also
+                // means this tile's O holds every earlier P.V product
+                if (grp == 0) {
+                    if (p_cnt > 0 && !(ok = wait(bars.pv_done[1], (p_cnt - 1) & 1))) break;
+                } else {
+                    if (!(ok = wait(bars.pv_done[0], p_cnt & 1))) break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, rescale)) {
+                    const float a = rescale ? alpha : 1.f;
+#pragma unroll
+                    for (int c = 0; c < D; c += 16) {
+                        uint32_t r[16];
+                        tmem_ld16(tO + c, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
+                        tmem_st16(tO + c, r);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c + 32 <= BN / 2; c += 32) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = pk[c + e];
+                    tmem_st32(tP + c, r);
+                }
+                if constexpr ((BN / 2) % 32 != 0) {
+                    constexpr int c = (BN / 2) / 32 * 32;
+                    uint32_t r[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[e] = pk[c + e];
+                    tmem_st16(tP + c, r);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_addr(bars.p_full[grp]));
+                ++p_cnt;
+            }
+            if (!ok) break;
+
+            // epilogue: wait for this tile's last P.V, then O / l -> bf16 -> HBM
+            if (!(ok = wait(bars.pv_done[grp], (p_cnt - 1) & 1))) break;
+            tc_fence_after();
+            const int q_row = q0 + grp * BM + row;
+            const bool store = q_row < seg0 + seg_len;
+            const float inv_l = 1.f / l_run;
+            __nv_bfloat16 *dst = out + (int64_t)q_row * out_stride + (int64_t)head * D;
+#pragma unroll
+            for (int c = 0; c < D; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(tO + c, r);
+                tmem_wait_ld();
+                uint32_t o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    o[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+                if (store) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+                    d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_addr(bars.o_free[grp]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// [T, H*D] bf16 rows with a token stride, read as 16-column slabs of `rows` rows, 32-byte swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int D, int64_t stride, int rows)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)H * D, (cuuint64_t)(T > 0 ? T : 1)};
+    cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
+    cuuint32_t box[2] = {16, (cuuint32_t)rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const void *q, const void *k, const void *v, int64_t T, int H, int64_t qs, int64_t ks,
+                     int64_t vs, void *out, int64_t os, float scale_log2, const WsHeader *hdr, const Item *items,
+                     int64_t max_items, int num_sms, int32_t *status, cudaStream_t stream)
+{
+    using C = LongCfg<D>;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, q, T, H, D, qs, BM) || !make_map(&mk, k, T, H, D, ks, C::BN) ||
+        !make_map(&mv, v, T, H, D, vs, C::BN))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(attn_long_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    const unsigned blocks = (unsigned)(max_items < num_sms ? max_items : num_sms);
+    if (blocks == 0) return cudaSuccess;
+    LaunchScope scope("attn_long", stream);
+    attn_long_kernel<D><<<blocks, kThreads, C::SMEM, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16 *>(out), os,
+                                                               scale_log2, hdr, items, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int attn_long_bm() { return 2 * BM; }
+
+bool attn_long_supports(int D) { return D == 32 || D == 64 || D == 80 || D == 96 || D == 128; }
+
+cudaError_t launch_attn_long(const void *q, const void *k, const void *v, int64_t T, int H, int64_t q_stride,
+                             int64_t k_stride, int64_t v_stride, void *out, int64_t out_stride, int D,
+                             float scale_log2, const WsHeader *hdr, const Item *items, int64_t max_items_long,
+                             int num_sms, int32_t *status, cudaStream_t stream)
+{
+    switch (D) {
+        case 32: return launch_d<32>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stream);
+        case 64: return launch_d<64>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stream);
+        case 80: return launch_d<80>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stream);
+        case 96: return launch_d<96>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stream);
+        case 128: return launch_d<128>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace vit

@@ -71,4 +71,9 @@ cudaError_t launch_attn_short(const void *q, const void *k, const void *v, int64
                               int D, float scale_log2, const WsHeader *hdr, const Item *items,
                               int64_t max_items_short, int num_sms, cudaStream_t stream);
 
+cudaError_t launch_attn_long(const void *q, const void *k, const void *v, int64_t T, int H, int64_t q_stride,
+                             int64_t k_stride, int64_t v_stride, void *out, int64_t out_stride, int D,
+                             float scale_log2, const WsHeader *hdr, const Item *items, int64_t max_items_long,
+                             int num_sms, int32_t *status, cudaStream_t stream);
+
 }  // namespace vit
