@@ -54,6 +54,20 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_max(x: float, device) -> float:
+    """Max over ranks (identity without an initialised process group)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's useful flops over the slowest rank's step time."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ clocks during the timed region
 
 class ClockSampler:
@@ -168,16 +182,12 @@ def load_traffic(kernel: str, workload: str):
     return e.get("bytes_per_launch")
 
 
-def kernel_algorithmic_flops(w: wl.Workload, kernel: str) -> float:
-    """Useful flops a kernel processes per step: 4 L^2 H D over the segments it owns."""
+def kernel_algorithmic_flops(w: wl.Workload, kernel: str, short_max: int) -> float:
+    """Useful flops a kernel processes per step: 4 L^2 H D over the segments it owns
+    (attn_long: segments longer than short_max tokens; attn_short: the rest)."""
     L = w.lengths.astype(np.float64)
-    short_max = SHORT_MAX_BY_KERNEL.get(kernel)
-    if short_max is not None:
-        L = L[L <= short_max] if kernel == "attn_short" else L[L > short_max]
+    L = L[L > short_max] if kernel == "attn_long" else L[L <= short_max]
     return float(4.0 * np.sum(L * L) * w.heads * w.head_dim)
-
-
-SHORT_MAX_BY_KERNEL = {"attn_short": float("inf"), "attn_long": float("inf")}
 
 
 def cpu_baseline_sample(w: wl.Workload, t: dict, target_s: float):
@@ -269,11 +279,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     barrier()
     launches = vit.launch_count() - launches0
-    ms = total_ms / args.steps
-    if world > 1:
-        m = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(m, op=torch.distributed.ReduceOp.MAX)
-        ms = float(m.item())
+    ms = reduce_max(total_ms / args.steps, device)
     clk = clocks.summary()
 
     # ---- end to end through the public API from pinned host memory
@@ -294,17 +300,13 @@ def run_ours(args, rank, world, local):
         e2e_step(vit, w, host, device, stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        m = torch.tensor([e2e_ms], device=device)
-        torch.distributed.all_reduce(m, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(m.item())
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, device)
 
     if rank != 0:
         return
     peaks, peaks_src = load_peaks()
     flops = w.useful_flops
-    value = flops * world / (ms * 1e-3) / 1e12
+    value = job_tflops(flops, world, ms)
     kernels = {name: {"launches": n, "avg_ms": tot / max(n, 1)} for name, (n, tot) in kt.items()}
     dom = max(kt.items(), key=lambda kv: kv[1][1])[0] if kt else None
     roofline = None
@@ -312,7 +314,9 @@ def run_ours(args, rank, world, local):
         n, tot = kt[dom]
         avg_s = tot / n * 1e-3
         if dom.startswith("attn"):
-            alg = kernel_algorithmic_flops(w, dom)
+            short_max = vit.set_short_segment_max(128)
+            vit.set_short_segment_max(short_max)
+            alg = kernel_algorithmic_flops(w, dom, short_max)
             peak = peaks["bf16_tflops_sustained"]
             achieved = alg / avg_s / 1e12
             roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -337,7 +341,7 @@ def run_ours(args, rank, world, local):
         "tokens_per_s": T * world / (ms * 1e-3),
         "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
         "clocks": clk,
-        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "kernels": kernels,

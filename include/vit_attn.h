@@ -182,6 +182,16 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
 int vit_set_short_segment_max(int short_max);
 
 /*
+ * Test hook for the failure path. While enabled (1), the long-segment kernel
+ * skips its V tile loads, so the MMA warp's bounded wait expires: the call
+ * stores VIT_ERR_TIMEOUT in status_dev, every warp gives up, the kernel frees
+ * its tensor memory and exits, and the CUDA context stays usable. No fault,
+ * trap or unbounded wait is involved. Outputs of such a call are undefined.
+ * Returns the previous setting. Never enable it outside tests.
+ */
+int vit_debug_stall_long_kernel(int enable);
+
+/*
  * Synchronise `stream`, then read the status word. Returns VIT_OK, the first
  * device-detected error code stored there, or VIT_ERR_CUDA when the stream or
  * the copy failed. The only call of the compute path that blocks the host.

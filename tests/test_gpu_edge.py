@@ -158,3 +158,27 @@ def test_launches_are_counted_and_timed():
         vit.kernel_timing(False)
     assert vit.launch_count() - n0 >= 2
     assert "schedule" in rec and all(ms >= 0 for _, ms in rec.values())
+
+
+def test_long_kernel_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that can never complete (V is never loaded) must end in
+    VIT_ERR_TIMEOUT within its clock budget; afterwards the same process
+    computes correct results again."""
+    w, t, cu, (q, k, v) = _inputs([600, 300], 2, 80, seed=7)
+    prev = vit.set_short_segment_max(0)
+    try:
+        status = vit.new_status()
+        vit.debug_stall_long_kernel(True)
+        try:
+            vit.varlen_attn(q, k, v, cu, w.max_seqlen, status=status)
+            code = vit.read_status(status)
+        finally:
+            vit.debug_stall_long_kernel(False)
+        assert code == -13
+        status2 = vit.new_status()
+        out = vit.varlen_attn(q, k, v, cu, w.max_seqlen, status=status2)
+        assert vit.read_status(status2) == 0
+    finally:
+        vit.set_short_segment_max(prev)
+    ref = oracle.attention(*(oracle.widen(wl.bf16_bits(t[n])) for n in ("q", "k", "v")), w.cu_seqlens)
+    assert_close(out, ref, what="after timeout")

@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
             L.vit_read_status.argtypes = [vp, vp]
             L.vit_set_short_segment_max.argtypes = [i32]
             L.vit_set_short_segment_max.restype = i32
+            L.vit_debug_stall_long_kernel.argtypes = [i32]
+            L.vit_debug_stall_long_kernel.restype = i32
             L.vit_launch_count.restype = i64
             L.vit_kernel_timing.argtypes = [i32]
             L.vit_kernel_timing_read.argtypes = [ctypes.POINTER(_KernelTime), i32]
@@ -189,6 +191,11 @@ def set_short_segment_max(short_max: int) -> int:
     """Segments longer than short_max go to the tcgen05 long-segment kernel (default 128).
     Returns the previous value."""
     return int(lib().vit_set_short_segment_max(int(short_max)))
+
+
+def debug_stall_long_kernel(enable: bool) -> bool:
+    """Test hook: make the long-segment kernel's bounded waits expire (VIT_ERR_TIMEOUT)."""
+    return bool(lib().vit_debug_stall_long_kernel(1 if enable else 0))
 
 
 def launch_count() -> int:

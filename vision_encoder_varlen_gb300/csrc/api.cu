@@ -55,6 +55,8 @@ constexpr int64_t kMaxTokens = (int64_t)1 << 31;
 
 // Segments longer than this run on the tcgen05 long-segment kernel.
 std::atomic<int> g_short_max{128};
+// Test hook: when set, the long-segment kernel never loads V, so its bounded waits expire.
+std::atomic<int> g_stall_v{0};
 
 }  // namespace
 
@@ -186,7 +188,7 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
     const int64_t longest = cu_seqlens ? (int64_t)max_seqlen : T / B;
     if (longest > sp.short_max) {
         e = launch_attn_long(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, D, scale_log2, hdr, items,
-                             max_items(T, H, B, sp.bm_long), sms, status_dev, s);
+                             max_items(T, H, B, sp.bm_long), sms, status_dev, g_stall_v.load(), s);
         if (e != cudaSuccess) return VIT_ERR_CUDA;
     }
     if (sp.short_max > 0) {
@@ -194,6 +196,11 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
                               max_items(T, H, B, sp.bm_short), sms, s);
     }
     return from_cuda(e);
+}
+
+int vit_debug_stall_long_kernel(int enable)
+{
+    return g_stall_v.exchange(enable ? 1 : 0);
 }
 
 int vit_set_short_segment_max(int short_max)

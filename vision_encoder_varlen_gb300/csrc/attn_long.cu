@@ -8,7 +8,9 @@
 //
 // One work item = (segment, head, 256 query rows) = two 128-row Q tiles that
 // share every K/V tile the TMA warp streams in. Persistent CTAs (one per SM)
-// walk the scheduler's longest-first list. Warp roles (320 threads):
+// walk the scheduler's longest-first list. Three warpgroups (384 threads,
+// launched at 168 registers; setmaxnreg lowers the control warpgroup to 96
+// and raises the two softmax warpgroups to 200):
 //   warp 0      TMA producer: Q tiles per item, K and V tiles into a ring of
 //               STAGES slots; 16-column (32-byte) slabs with 32-byte swizzle,
 //               so any head_dim that is a multiple of 16 maps exactly.
@@ -18,8 +20,9 @@
 //               issued in the order QK0(j+1), PV0(j), QK1(j+1), PV1(j) so the
 //               tensor pipe always has the other tile's work queued while a
 //               softmax group turns S into P.
-//   warps 2-5   softmax group 0 (tile 0), one TMEM lane = one query row per
-//   warps 6-9   softmax group 1 (tile 1)  thread: row max, lazy rescaling of
+//   warps 2-3   idle (complete the control warpgroup)
+//   warps 4-7   softmax group 0 (tile 0), one TMEM lane = one query row per
+//   warps 8-11  softmax group 1 (tile 1)  thread: row max, lazy rescaling of
 //               O (only when the max grows by more than 2^8), exp2 with the
 //               scale folded in, row sum, P -> bf16 into a P region of TMEM
 //               shared by both tiles, and the epilogue O / l -> bf16 -> HBM.
@@ -38,7 +41,11 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;              // 65536 / 384, rounded down to a multiple of 8
+constexpr int kCtrlRegs = 96;                 // control warpgroup after setmaxnreg.dec
+constexpr int kSoftmaxRegs = 200;             // softmax warpgroups after setmaxnreg.inc
+static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split exceeds the launch pool");
 constexpr int BM = 128;                       // rows per Q tile; two tiles per item
 constexpr long long kWaitBudget = 4000000000ll;   // clock cycles before a wait gives up (~2 s)
 
@@ -72,11 +79,11 @@ struct Bars {
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_addr(&b); }
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
 attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out, int64_t out_stride,
                  float scale_log2, const WsHeader *__restrict__ hdr, const Item *__restrict__ items,
-                 int32_t *status)
+                 int32_t *status, int stall_v)
 {
     using C = LongCfg<D>;
     constexpr int BN = C::BN, ST = C::STAGES, NSLAB = C::NSLAB;
@@ -128,7 +135,13 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         fail();
         return false;
     };
+    // softmax warps run warp-collective tcgen05.ld/st after their waits: all 32 lanes
+    // either go on together or give up together
+    auto wait_warp = [&](const uint64_t &b, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait(b, parity)) != 0;
+    };
 
+    if (warp < 4) regs_dec<kCtrlRegs>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -136,6 +149,9 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             uint32_t g = 0, q_it = 0;
+            // parity + 1 of the last load issued on each barrier (0 = none), for the abort drain
+            uint32_t q_pend = 0, k_pend[ST], v_pend[ST];
+            for (int s = 0; s < ST; ++s) k_pend[s] = v_pend[s] = 0;
             bool ok = true;
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++q_it) {
                 const Item item = items[it];
@@ -147,6 +163,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     for (int s = 0; s < NSLAB; ++s)
                         tma_load_2d(smem_addr(base + C::OFF_Q + i * C::Q_TILE + s * C::Q_SLAB), &tm_q,
                                     head * D + 16 * s, q0 + BM * i, bar_addr(bars.q_full));
+                q_pend = (q_it & 1) + 1;
                 for (int j = 0; j < n_kv; ++j, ++g) {
                     const int st = g % ST;
                     if (g >= (uint32_t)ST && !(ok = wait(bars.kv_empty[st], (g / ST - 1) & 1))) break;
@@ -155,19 +172,23 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     for (int s = 0; s < NSLAB; ++s)
                         tma_load_2d(smem_addr(base + C::OFF_K + st * C::KV_TILE + s * C::KV_SLAB), &tm_k,
                                     head * D + 16 * s, row, bar_addr(bars.k_full[st]));
+                    k_pend[st] = ((g / ST) & 1) + 1;
+                    if (stall_v) continue;          // test hook: V never arrives, the MMA wait expires
                     mbar_arrive_expect_tx(bar_addr(bars.v_full[st]), C::KV_TILE);
                     for (int s = 0; s < NSLAB; ++s)
                         tma_load_2d(smem_addr(base + C::OFF_V + st * C::KV_TILE + s * C::KV_SLAB), &tm_v,
                                     head * D + 16 * s, row, bar_addr(bars.v_full[st]));
+                    v_pend[st] = ((g / ST) & 1) + 1;
                 }
             }
             if (!ok) {
-                // let copies already issued land before the CTA's shared memory goes away
+                // let every copy already issued land before this CTA's shared memory is released
+                // (loads that completed earlier return at once; short budget, abort flag ignored)
+                const int never = 0;
+                if (q_pend) mbar_wait(bar_addr(bars.q_full), q_pend - 1, &never, 20000000ll);
                 for (int s = 0; s < ST; ++s) {
-                    mbar_wait(bar_addr(bars.k_full[s]), 0, (const volatile int *)&s_abort, 0);
-                }
-                const long long t0 = clock64();
-                while (clock64() - t0 < 2000000) {
+                    if (k_pend[s]) mbar_wait(bar_addr(bars.k_full[s]), k_pend[s] - 1, &never, 20000000ll);
+                    if (v_pend[s]) mbar_wait(bar_addr(bars.v_full[s]), v_pend[s] - 1, &never, 20000000ll);
                 }
             }
         }
@@ -249,9 +270,10 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mma_commit(bar_addr(bars.drain));
             mbar_wait(bar_addr(bars.drain), 0, (const volatile int *)&s_abort, ok ? kWaitBudget : 200000000ll);
         }
-    } else {
+    } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax groups
-        const int grp = (warp - 2) >> 2;                       // 0 or 1: which Q tile
+        regs_inc<kSoftmaxRegs>();
+        const int grp = (warp - 4) >> 2;                       // 0 or 1: which Q tile
         const int quarter = warp & 3;                          // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;                   // row of the tile = TMEM lane
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -268,7 +290,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             float m_run = -INFINITY, l_run = 0.f;
 
             for (int j = 0; j < n_kv && ok; ++j) {
-                if (!(ok = wait(bars.s_full[grp], s_cnt & 1))) break;
+                if (!(ok = wait_warp(bars.s_full[grp], s_cnt & 1))) break;
                 tc_fence_after();
                 float s[BN];
 #pragma unroll
@@ -314,9 +336,9 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // the shared P region is free once the previous P.V product finished; that also
                 // means this tile's O holds every earlier P.V product
                 if (grp == 0) {
-                    if (p_cnt > 0 && !(ok = wait(bars.pv_done[1], (p_cnt - 1) & 1))) break;
+                    if (p_cnt > 0 && !(ok = wait_warp(bars.pv_done[1], (p_cnt - 1) & 1))) break;
                 } else {
-                    if (!(ok = wait(bars.pv_done[0], p_cnt & 1))) break;
+                    if (!(ok = wait_warp(bars.pv_done[0], p_cnt & 1))) break;
                 }
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, rescale)) {
@@ -354,7 +376,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (!ok) break;
 
             // epilogue: wait for this tile's last P.V, then O / l -> bf16 -> HBM
-            if (!(ok = wait(bars.pv_done[grp], (p_cnt - 1) & 1))) break;
+            if (!(ok = wait_warp(bars.pv_done[grp], (p_cnt - 1) & 1))) break;
             tc_fence_after();
             const int q_row = q0 + grp * BM + row;
             const bool store = q_row < seg0 + seg_len;
@@ -422,7 +444,7 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int D, int64_t 
 template <int D>
 cudaError_t launch_d(const void *q, const void *k, const void *v, int64_t T, int H, int64_t qs, int64_t ks,
                      int64_t vs, void *out, int64_t os, float scale_log2, const WsHeader *hdr, const Item *items,
-                     int64_t max_items, int num_sms, int32_t *status, cudaStream_t stream)
+                     int64_t max_items, int num_sms, int32_t *status, int stall_v, cudaStream_t stream)
 {
     using C = LongCfg<D>;
     CUtensorMap mq, mk, mv;
@@ -431,11 +453,16 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, int64_t T, int
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(attn_long_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    // the setmaxnreg split assumes exactly this launch budget; refuse anything else rather than wait on it
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attn_long_kernel<D>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
     const unsigned blocks = (unsigned)(max_items < num_sms ? max_items : num_sms);
     if (blocks == 0) return cudaSuccess;
     LaunchScope scope("attn_long", stream);
     attn_long_kernel<D><<<blocks, kThreads, C::SMEM, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16 *>(out), os,
-                                                               scale_log2, hdr, items, status);
+                                                               scale_log2, hdr, items, status, stall_v);
     return cudaGetLastError();
 }
 
@@ -448,14 +475,14 @@ bool attn_long_supports(int D) { return D == 32 || D == 64 || D == 80 || D == 96
 cudaError_t launch_attn_long(const void *q, const void *k, const void *v, int64_t T, int H, int64_t q_stride,
                              int64_t k_stride, int64_t v_stride, void *out, int64_t out_stride, int D,
                              float scale_log2, const WsHeader *hdr, const Item *items, int64_t max_items_long,
-                             int num_sms, int32_t *status, cudaStream_t stream)
+                             int num_sms, int32_t *status, int stall_v, cudaStream_t stream)
 {
     switch (D) {
-        case 32: return launch_d<32>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stream);
-        case 64: return launch_d<64>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stream);
-        case 80: return launch_d<80>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stream);
-        case 96: return launch_d<96>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stream);
-        case 128: return launch_d<128>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stream);
+        case 32: return launch_d<32>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stall_v, stream);
+        case 64: return launch_d<64>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stall_v, stream);
+        case 80: return launch_d<80>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stall_v, stream);
+        case 96: return launch_d<96>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stall_v, stream);
+        case 128: return launch_d<128>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stall_v, stream);
         default: return cudaErrorInvalidValue;
     }
 }

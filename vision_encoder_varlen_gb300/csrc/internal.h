@@ -74,6 +74,6 @@ cudaError_t launch_attn_short(const void *q, const void *k, const void *v, int64
 cudaError_t launch_attn_long(const void *q, const void *k, const void *v, int64_t T, int H, int64_t q_stride,
                              int64_t k_stride, int64_t v_stride, void *out, int64_t out_stride, int D,
                              float scale_log2, const WsHeader *hdr, const Item *items, int64_t max_items_long,
-                             int num_sms, int32_t *status, cudaStream_t stream);
+                             int num_sms, int32_t *status, int stall_v, cudaStream_t stream);
 
 }  // namespace vit
