@@ -171,6 +171,38 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
                              void *out, int64_t out_stride, void *workspace, size_t workspace_bytes,
                              int32_t *status_dev, vit_stream_t stream);
 
+/* Size of the fixed device scratch array behind vit_varlen_attn_noalloc (per GPU). */
+#define VIT_NOALLOC_WORKSPACE_BYTES (4u << 20)
+
+/*
+ * vit_varlen_attn for callers that cannot allocate device memory. The pages
+ * have no counterpart of this call: it exists for code that runs where new
+ * device allocations are not allowed or not possible, such as a serving loop
+ * whose memory pool is frozen after warm-up, a plugin that is handed only its
+ * input and output pointers, or a C caller with no allocator of its own.
+ *
+ * Arguments, layouts and results are those of vit_varlen_attn without the
+ * workspace pair: the scheduler's work list lives instead in a static device
+ * array of VIT_NOALLOC_WORKSPACE_BYTES (4 MiB) inside this library, which
+ * every GPU that loads the library keeps until the process exits. The call
+ * itself allocates nothing (no cudaMalloc, no library allocator).
+ *   - Limit: sizes whose work list needs more than VIT_NOALLOC_WORKSPACE_BYTES
+ *     (vit_varlen_attn_workspace_size(T, H, B, D) > 4 MiB; roughly
+ *     H * (T/64 + B) > 262000 work items) return VIT_ERR_WORKSPACE_TOO_SMALL
+ *     and launch nothing; use vit_varlen_attn with your own workspace there.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array, and it keeps whatever the
+ *     previous call left there; every call rewrites what it reads, so nothing
+ *     needs clearing, but two calls that overlap on the GPU (different streams
+ *     without ordering between them) race on it and must not be issued.
+ */
+vit_status_t vit_varlen_attn_noalloc(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                     int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                                     const int32_t *cu_seqlens, int B, int max_seqlen, float scale,
+                                     void *out, int64_t out_stride, int32_t *status_dev, vit_stream_t stream);
+
 /*
  * Kernel split of vit_varlen_attn: segments longer than `short_max` tokens run
  * on the tcgen05/TMEM long-segment kernel (256 query rows per work item), the
