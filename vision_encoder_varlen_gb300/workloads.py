@@ -130,6 +130,10 @@ def make_config(idx: int) -> Workload:
         grids = ((256, 256),) + _uniform_grids(rng, 7, 8, 32, 8, 32)
         return Workload("mixed_256x256+7small_h16_d80_qknorm_max131072", grids, 16, 80, True,
                         max_seqlen_meta=131072, seed=seed)
+    if idx == 6:
+        # not one of the five study shapes: a single 128x128 image used for profiler captures
+        # (168 MB of q/k/v/out, above the 129 MB L2, ~1.5 ms of attention)
+        return Workload("profile_128x128_h16_d80_qknorm", ((128, 128),), 16, 80, True, seed=seed)
     raise ValueError(f"no workload {idx}")
 
 
