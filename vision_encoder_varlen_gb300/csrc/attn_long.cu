@@ -9,18 +9,18 @@
 // One work item = (segment, head, 256 query rows) = two 128-row Q tiles that
 // share every K/V tile the TMA warp streams in. Persistent CTAs (one per SM)
 // walk the scheduler's longest-first list. Three warpgroups (384 threads,
-// launched at 168 registers; setmaxnreg lowers the control warpgroup to 96
-// and raises the two softmax warpgroups to 200):
+// launched at 168 registers; setmaxnreg lowers the control warpgroup to 88
+// and raises the two softmax warpgroups to 208):
 //   warp 0      TMA producer: Q tiles per item, K and V tiles into a ring of
 //               STAGES slots; 16-column (32-byte) slabs with 32-byte swizzle,
 //               so any head_dim that is a multiple of 16 maps exactly.
-//   warp 1      TMEM owner and single-thread MMA issuer:
+//   warp 1      TMEM owner; lane 0 issues the MMAs of Q tile 0
+//   warp 2      lane 0 issues the MMAs of Q tile 1
 //                 S_i = Q_i K^T     (SS MMA, M=128, N=BN, K=D)   into TMEM
 //                 O_i += P V        (TS MMA, A=P from TMEM, B=V MN-major)
-//               issued in the order QK0(j+1), PV0(j), QK1(j+1), PV1(j) so the
-//               tensor pipe always has the other tile's work queued while a
-//               softmax group turns S into P.
-//   warps 2-3   idle (complete the control warpgroup)
+//               each issuer orders QK(j+1) before PV(j), so S of the next key
+//               tile is computed while its softmax group turns S into P.
+//   warp 3      idle (completes the control warpgroup)
 //   warps 4-7   softmax group 0 (tile 0), one TMEM lane = one query row per
 //   warps 8-11  softmax group 1 (tile 1)  thread: row max, lazy rescaling of
 //               O (only when the max grows by more than 2^8), exp2 with the
@@ -43,8 +43,8 @@ using namespace sm100;
 
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;              // 65536 / 384, rounded down to a multiple of 8
-constexpr int kCtrlRegs = 96;                 // control warpgroup after setmaxnreg.dec
-constexpr int kSoftmaxRegs = 200;             // softmax warpgroups after setmaxnreg.inc
+constexpr int kCtrlRegs = 88;                 // control warpgroup after setmaxnreg.dec
+constexpr int kSoftmaxRegs = 208;             // softmax warpgroups after setmaxnreg.inc
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split exceeds the launch pool");
 constexpr int BM = 128;                       // rows per Q tile; two tiles per item
 constexpr long long kWaitBudget = 4000000000ll;   // clock cycles before a wait gives up (~2 s)
@@ -73,7 +73,7 @@ struct Bars {
     uint64_t q_full, q_empty;
     uint64_t k_full[3], v_full[3], kv_empty[3];
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
-    uint64_t drain;
+    uint64_t drain[2];
 };
 
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_addr(&b); }
@@ -99,11 +99,11 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (threadIdx.x == 0) {
         s_abort = 0;
         mbar_init(bar_addr(bars.q_full), 1);
-        mbar_init(bar_addr(bars.q_empty), 1);
+        mbar_init(bar_addr(bars.q_empty), 2);            // one commit from each MMA issuer
         for (int s = 0; s < ST; ++s) {
             mbar_init(bar_addr(bars.k_full[s]), 1);
             mbar_init(bar_addr(bars.v_full[s]), 1);
-            mbar_init(bar_addr(bars.kv_empty[s]), 1);
+            mbar_init(bar_addr(bars.kv_empty[s]), 2);    // one commit from each MMA issuer
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(bars.s_full[i]), 1);
@@ -112,7 +112,8 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(bar_addr(bars.pv_done[i]), 1);
             mbar_init(bar_addr(bars.o_free[i]), 4);
         }
-        mbar_init(bar_addr(bars.drain), 1);
+        mbar_init(bar_addr(bars.drain[0]), 1);
+        mbar_init(bar_addr(bars.drain[1]), 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -149,9 +150,9 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             uint32_t g = 0, q_it = 0;
-            // parity + 1 of the last load issued on each barrier (0 = none), for the abort drain
-            uint32_t q_pend = 0, k_pend[ST], v_pend[ST];
-            for (int s = 0; s < ST; ++s) k_pend[s] = v_pend[s] = 0;
+            // parity + 1 of the last load issued on each barrier (0 = none), for the abort drain;
+            // two bits per stage, kept in registers
+            uint32_t q_pend = 0, k_pend = 0, v_pend = 0;
             bool ok = true;
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++q_it) {
                 const Item item = items[it];
@@ -172,13 +173,13 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     for (int s = 0; s < NSLAB; ++s)
                         tma_load_2d(smem_addr(base + C::OFF_K + st * C::KV_TILE + s * C::KV_SLAB), &tm_k,
                                     head * D + 16 * s, row, bar_addr(bars.k_full[st]));
-                    k_pend[st] = ((g / ST) & 1) + 1;
+                    k_pend = (k_pend & ~(3u << (2 * st))) | ((((g / ST) & 1) + 1) << (2 * st));
                     if (stall_v) continue;          // test hook: V never arrives, the MMA wait expires
                     mbar_arrive_expect_tx(bar_addr(bars.v_full[st]), C::KV_TILE);
                     for (int s = 0; s < NSLAB; ++s)
                         tma_load_2d(smem_addr(base + C::OFF_V + st * C::KV_TILE + s * C::KV_SLAB), &tm_v,
                                     head * D + 16 * s, row, bar_addr(bars.v_full[st]));
-                    v_pend[st] = ((g / ST) & 1) + 1;
+                    v_pend = (v_pend & ~(3u << (2 * st))) | ((((g / ST) & 1) + 1) << (2 * st));
                 }
             }
             if (!ok) {
@@ -186,89 +187,91 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // (loads that completed earlier return at once; short budget, abort flag ignored)
                 const int never = 0;
                 if (q_pend) mbar_wait(bar_addr(bars.q_full), q_pend - 1, &never, 20000000ll);
+#pragma unroll
                 for (int s = 0; s < ST; ++s) {
-                    if (k_pend[s]) mbar_wait(bar_addr(bars.k_full[s]), k_pend[s] - 1, &never, 20000000ll);
-                    if (v_pend[s]) mbar_wait(bar_addr(bars.v_full[s]), v_pend[s] - 1, &never, 20000000ll);
+                    const uint32_t kp = (k_pend >> (2 * s)) & 3u, vp = (v_pend >> (2 * s)) & 3u;
+                    if (kp) mbar_wait(bar_addr(bars.k_full[s]), kp - 1, &never, 20000000ll);
+                    if (vp) mbar_wait(bar_addr(bars.v_full[s]), vp - 1, &never, 20000000ll);
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 1 issues every MMA of Q tile 0, warp 2 every MMA of Q tile 1. A single issuer's
+        // serial chain (barrier checks of ~100 cycles each, fences, commits, the MMAs) per key
+        // tile is about as long as the tensor work of that tile at head_dim 80, so one thread
+        // per tile halves it. Descriptors are precomputed 64-bit bases plus compile-time offsets
+        // (the address field is the low 14 bits and never carries); every barrier parity derives
+        // from one global key-tile counter. The two issuers share nothing but the K/V stage
+        // barriers (two-arrival kv_empty / q_empty); the order of P.V products on the shared
+        // P region is enforced by the softmax groups, which write P only after the other tile's
+        // previous P.V has completed.
         if (lane == 0) {
+            const int ti = warp - 1;                              // Q tile of this issuer
             constexpr uint32_t ID_QK = idesc_bf16(128, BN, 0, 0);
             constexpr uint32_t ID_PV = idesc_bf16(128, D, 0, 1);
-            const uint32_t tS[2] = {tmem + C::TS0, tmem + C::TS1};
-            const uint32_t tO[2] = {tmem + C::TO0, tmem + C::TO1};
+            constexpr uint32_t STAGE_STEP = C::KV_TILE >> 4;
+            const uint32_t tS = tmem + (ti ? C::TS1 : C::TS0);
+            const uint32_t tO = tmem + (ti ? C::TO1 : C::TO0);
             const uint32_t tP = tmem + C::TP;
-            const uint32_t q_base = smem_addr(base + C::OFF_Q);
-            const uint32_t k_base = smem_addr(base + C::OFF_K);
-            const uint32_t v_base = smem_addr(base + C::OFF_V);
-            uint32_t g = 0, item_cnt = 0;
-            uint32_t s_cnt[2] = {0, 0}, pv_cnt[2] = {0, 0};
+            const uint64_t dq = smem_desc(smem_addr(base + C::OFF_Q + ti * C::Q_TILE), 16, 256, 6);
+            const uint64_t dk0 = smem_desc(smem_addr(base + C::OFF_K), 16, 256, 6);
+            const uint64_t dv0 = smem_desc(smem_addr(base + C::OFF_V), C::KV_SLAB, 256, 6);
+            const uint64_t &b_sfree = bars.s_free[ti], &b_pfull = bars.p_full[ti], &b_ofree = bars.o_free[ti];
+            const uint32_t a_sfull = bar_addr(bars.s_full[ti]), a_pvdone = bar_addr(bars.pv_done[ti]);
+            uint32_t t = 0, item_cnt = 0;             // global key-tile counter, items done
             bool ok = true;
 
-            auto issue_qk = [&](int i, int st) {
-                const uint32_t qa = q_base + i * C::Q_TILE, ka = k_base + st * C::KV_TILE;
+            auto qk = [&](uint64_t dk) {
 #pragma unroll
                 for (int kk = 0; kk < NSLAB; ++kk)
-                    mma_ss(tS[i], smem_desc(qa + kk * C::Q_SLAB, 16, 256, 6), smem_desc(ka + kk * C::KV_SLAB, 16, 256, 6),
-                           ID_QK, kk > 0);
-                mma_commit(bar_addr(bars.s_full[i]));
-                ++s_cnt[i];
+                    mma_ss(tS, dq + (uint64_t)(kk * (C::Q_SLAB >> 4)), dk + (uint64_t)(kk * (C::KV_SLAB >> 4)), ID_QK,
+                           kk > 0 ? 1u : 0u);
+                mma_commit(a_sfull);
             };
-            auto issue_pv = [&](int i, int st, bool acc) {
-                const uint32_t va = v_base + st * C::KV_TILE;
+            auto pv = [&](uint64_t dv, uint32_t acc) {
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tO[i], tP + kk * 8, smem_desc(va + kk * 16 * 32, C::KV_SLAB, 256, 6), ID_PV,
-                           (acc || kk > 0) ? 1u : 0u);
-                mma_commit(bar_addr(bars.pv_done[i]));
-                ++pv_cnt[i];
+                    mma_ts(tO, tP + kk * 8, dv + (uint64_t)(kk * (512 >> 4)), ID_PV, kk > 0 ? 1u : acc);
+                mma_commit(a_pvdone);
             };
 
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_cnt) {
                 const Item item = items[it];
                 const int n_kv = (item.y + BN - 1) / BN;
+                uint32_t st = t % ST, ph = (t / ST) & 1;
                 if (!(ok = wait(bars.q_full, item_cnt & 1))) break;
-                // prologue: S0(0), S1(0)
-                if (!(ok = wait(bars.k_full[g % ST], (g / ST) & 1))) break;
-                for (int i = 0; i < 2 && ok; ++i) {
-                    if (s_cnt[i] > 0 && !(ok = wait(bars.s_free[i], (s_cnt[i] - 1) & 1))) break;
-                    tc_fence_after();
-                    issue_qk(i, g % ST);
-                }
-                if (!ok) break;
+                // prologue: S of the item's first key tile
+                if (!(ok = wait(bars.k_full[st], ph))) break;
+                if (t > 0 && !(ok = wait(b_sfree, (t - 1) & 1))) break;
+                tc_fence_after();
+                qk(dk0 + st * STAGE_STEP);
                 if (n_kv == 1) mma_commit(bar_addr(bars.q_empty));
-                for (int j = 0; j < n_kv && ok; ++j) {
-                    const uint32_t gj = g + j, st = gj % ST, st1 = (gj + 1) % ST;
-                    if (j + 1 < n_kv) {
-                        if (!(ok = wait(bars.k_full[st1], ((gj + 1) / ST) & 1))) break;
-                        if (!(ok = wait(bars.s_free[0], (s_cnt[0] - 1) & 1))) break;
+                for (int j = 0; j < n_kv; ++j) {
+                    const uint32_t u = t + j;                 // global index of this key tile
+                    const uint32_t st1 = (st + 1 == (uint32_t)ST) ? 0u : st + 1;
+                    const uint32_t ph1 = (st + 1 == (uint32_t)ST) ? ph ^ 1u : ph;
+                    if (j + 1 < n_kv) {                        // next tile's S as soon as this S was read
+                        if (!(ok = wait(bars.k_full[st1], ph1))) break;
+                        if (!(ok = wait(b_sfree, u & 1))) break;
                         tc_fence_after();
-                        issue_qk(0, st1);
-                    }
-                    if (!(ok = wait(bars.v_full[st], (gj / ST) & 1))) break;
-                    if (j == 0 && item_cnt > 0 && !(ok = wait(bars.o_free[0], (item_cnt - 1) & 1))) break;
-                    if (!(ok = wait(bars.p_full[0], pv_cnt[0] & 1))) break;
-                    tc_fence_after();
-                    issue_pv(0, st, j > 0);
-                    if (j + 1 < n_kv) {
-                        if (!(ok = wait(bars.s_free[1], (s_cnt[1] - 1) & 1))) break;
-                        tc_fence_after();
-                        issue_qk(1, st1);
+                        qk(dk0 + st1 * STAGE_STEP);
                         if (j + 2 == n_kv) mma_commit(bar_addr(bars.q_empty));
                     }
-                    if (j == 0 && item_cnt > 0 && !(ok = wait(bars.o_free[1], (item_cnt - 1) & 1))) break;
-                    if (!(ok = wait(bars.p_full[1], pv_cnt[1] & 1))) break;
+                    if (!(ok = wait(bars.v_full[st], ph))) break;
+                    if (j == 0 && item_cnt > 0 && !(ok = wait(b_ofree, (item_cnt - 1) & 1))) break;
+                    if (!(ok = wait(b_pfull, u & 1))) break;
                     tc_fence_after();
-                    issue_pv(1, st, j > 0);
+                    pv(dv0 + st * STAGE_STEP, j > 0 ? 1u : 0u);
                     mma_commit(bar_addr(bars.kv_empty[st]));
+                    st = st1;
+                    ph = ph1;
                 }
-                g += n_kv;
+                t += n_kv;
             }
-            // drain: nothing of ours may still be running when TMEM is freed
-            mma_commit(bar_addr(bars.drain));
-            mbar_wait(bar_addr(bars.drain), 0, (const volatile int *)&s_abort, ok ? kWaitBudget : 200000000ll);
+            // drain: nothing this thread issued may still be running when TMEM is freed
+            mma_commit(bar_addr(bars.drain[ti]));
+            mbar_wait(bar_addr(bars.drain[ti]), 0, (const volatile int *)&s_abort, ok ? kWaitBudget : 200000000ll);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax groups
@@ -292,15 +295,12 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int j = 0; j < n_kv && ok; ++j) {
                 if (!(ok = wait_warp(bars.s_full[grp], s_cnt & 1))) break;
                 tc_fence_after();
-                float s[BN];
+                // S row -> registers: all loads in flight, one wait
+                uint32_t sr[BN];
 #pragma unroll
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tS + c, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) s[c + e] = __uint_as_float(r[e]);
-                }
+                for (int c = 0; c < BN; c += 32) tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(sr + c));
+                tmem_wait_ld();
+                reg_fence(sr);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_addr(bars.s_free[grp]));
@@ -310,11 +310,19 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (kv_valid < BN) {
 #pragma unroll
                     for (int c = 0; c < BN; ++c)
-                        if (c >= kv_valid) s[c] = -INFINITY;
+                        if (c >= kv_valid) sr[c] = __float_as_uint(-INFINITY);
                 }
-                float mx = s[0];
+                // row max: 8 independent chains of 3-input max, then a tree
+                static_assert(BN % 16 == 0, "row max consumes 16 columns per step");
+                float m8[8];
 #pragma unroll
-                for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+                for (int i = 0; i < 8; ++i) m8[i] = fmaxf(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
+#pragma unroll
+                for (int c = 16; c < BN; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        m8[i] = max3(m8[i], __uint_as_float(sr[c + 2 * i]), __uint_as_float(sr[c + 2 * i + 1]));
+                const float mx = fmaxf(max3(m8[0], m8[1], m8[2]), max3(max3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
                 const float m_tile = mx * scale_log2;
                 float alpha = 1.f;
                 if (m_tile > m_run + 8.f) {                    // lazy rescale: only when the max grows by > 2^8
@@ -322,16 +330,23 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     m_run = m_tile;
                 }
                 const bool rescale = (j > 0) && (alpha != 1.f);
+                // p = exp2(s * scale*log2(e) - m): pairs through the f32x2 FMA, row sum in f32x2 adds
                 uint32_t pk[BN / 2];
-                float sum = 0.f;
+                const uint64_t sc2 = f2_splat(scale_log2), nm2 = f2_splat(-m_run);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int c = 0; c < BN; c += 2) {
-                    const float p0 = ex2(fmaf(s[c], scale_log2, -m_run));
-                    const float p1 = ex2(fmaf(s[c + 1], scale_log2, -m_run));
-                    sum += p0 + p1;
+                    float x0, x1;
+                    f2_split(f2_fma(f2_from_u32(sr[c], sr[c + 1]), sc2, nm2), x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    uint64_t pp;
+                    asm("mov.b64 %0, {%1, %2};\n" : "=l"(pp) : "f"(p0), "f"(p1));
+                    acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], pp);
                     pk[c / 2] = pack_bf16x2(p0, p1);
                 }
-                l_run = l_run * alpha + sum;
+                float a0, a1;
+                f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+                l_run = l_run * alpha + (a0 + a1);
 
                 // the shared P region is free once the previous P.V product finished; that also
                 // means this tile's O holds every earlier P.V product
@@ -348,6 +363,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         uint32_t r[16];
                         tmem_ld16(tO + c, r);
                         tmem_wait_ld();
+                        reg_fence(r);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
                         tmem_st16(tO + c, r);
@@ -387,6 +403,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 uint32_t r[16];
                 tmem_ld16(tO + c, r);
                 tmem_wait_ld();
+                reg_fence(r);
                 uint32_t o[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
