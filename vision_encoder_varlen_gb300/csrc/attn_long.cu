@@ -24,9 +24,11 @@
 //   warps 4-7   softmax group 0 (tile 0), one TMEM lane = one query row per
 //   warps 8-11  softmax group 1 (tile 1)  thread: row max, lazy rescaling of
 //               O (only when the max grows by more than 2^8), exp2 with the
-//               scale folded in, row sum, P -> bf16 into a P region of TMEM
-//               shared by both tiles, and the epilogue O / l -> bf16 -> HBM.
-// TMEM (512 columns): S0 | S1 | O0 | O1 | P.  Keys past the segment end are
+//               scale folded in, row sum, P -> bf16 into the tile's own P
+//               region of TMEM, and the epilogue O / l -> bf16 -> HBM.
+// TMEM (512 columns): S0 | S1 | O0 | O1 | P0 | P1; the key tile BN is the
+// largest that fits (128 for head_dim <= 64, 112 for 80, 96 for 96, 80 for
+// 128), so the two tiles never wait for each other.  Keys past the segment end are
 // masked to -inf (they contribute exactly 0), query rows past it are never
 // stored, rows past T are zero-filled by TMA: no item reads or writes any
 // other segment's results. Every wait is bounded; a wait that expires sets
@@ -50,7 +52,9 @@ constexpr int BM = 128;                       // rows per Q tile; two tiles per 
 constexpr long long kWaitBudget = 4000000000ll;   // clock cycles before a wait gives up (~2 s)
 
 template <int D> struct LongCfg {
-    static constexpr int BN = (D <= 96) ? 128 : 96;       // keys per tile
+    // keys per tile: the largest multiple of 16 (at most 128) with S0, S1 (BN columns each),
+    // O0, O1 (D each) and separate P0, P1 (BN/2 each) inside the 512 TMEM columns
+    static constexpr int BN = ((512 - 2 * D) / 3 / 16 * 16 > 128) ? 128 : (512 - 2 * D) / 3 / 16 * 16;
     static constexpr int STAGES = 3;
     static constexpr int NSLAB = D / 16;
     static constexpr int Q_SLAB = BM * 32;                 // bytes of one 16-column slab of a Q tile
@@ -64,9 +68,12 @@ template <int D> struct LongCfg {
     // > half of the SM's shared memory: exactly one CTA (one TMEM owner) per SM
     static constexpr int SMEM = (DATA + 1024 > 118 * 1024) ? DATA + 1024 : 118 * 1024;
     // TMEM columns
-    static constexpr int TS0 = 0, TS1 = BN, TO0 = 2 * BN, TO1 = 2 * BN + D, TP = 2 * BN + 2 * D;
-    static_assert(TP + BN / 2 <= 512, "TMEM budget");
-    static_assert(D % 16 == 0 && BN % 32 == 0, "tile shapes");
+    // TMEM columns; every region starts on a 16-column boundary, P1 on an 8-column one,
+    // and every TMEM access below is naturally aligned to its own width
+    static constexpr int TS0 = 0, TS1 = BN, TO0 = 2 * BN, TO1 = 2 * BN + D, TP0 = 2 * BN + 2 * D;
+    static constexpr int TP1 = (TP0 + BN / 2 + 7) / 8 * 8;
+    static_assert(TP1 + BN / 2 <= 512, "TMEM budget");
+    static_assert(D % 16 == 0 && BN % 16 == 0 && (BN / 2) % 8 == 0, "tile shapes");
 };
 
 struct Bars {
@@ -203,9 +210,8 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // per tile halves it. Descriptors are precomputed 64-bit bases plus compile-time offsets
         // (the address field is the low 14 bits and never carries); every barrier parity derives
         // from one global key-tile counter. The two issuers share nothing but the K/V stage
-        // barriers (two-arrival kv_empty / q_empty); the order of P.V products on the shared
-        // P region is enforced by the softmax groups, which write P only after the other tile's
-        // previous P.V has completed.
+        // barriers (two-arrival kv_empty / q_empty); each softmax group rewrites its tile's P
+        // region only after that tile's previous P.V has completed.
         if (lane == 0) {
             const int ti = warp - 1;                              // Q tile of this issuer
             constexpr uint32_t ID_QK = idesc_bf16(128, BN, 0, 0);
@@ -213,7 +219,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             constexpr uint32_t STAGE_STEP = C::KV_TILE >> 4;
             const uint32_t tS = tmem + (ti ? C::TS1 : C::TS0);
             const uint32_t tO = tmem + (ti ? C::TO1 : C::TO0);
-            const uint32_t tP = tmem + C::TP;
+            const uint32_t tP = tmem + (ti ? C::TP1 : C::TP0);
             const uint64_t dq = smem_desc(smem_addr(base + C::OFF_Q + ti * C::Q_TILE), 16, 256, 6);
             const uint64_t dk0 = smem_desc(smem_addr(base + C::OFF_K), 16, 256, 6);
             const uint64_t dv0 = smem_desc(smem_addr(base + C::OFF_V), C::KV_SLAB, 256, 6);
@@ -282,7 +288,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         const uint32_t tS = t_lane + (grp ? C::TS1 : C::TS0);
         const uint32_t tO = t_lane + (grp ? C::TO1 : C::TO0);
-        const uint32_t tP = t_lane + C::TP;
+        const uint32_t tP = t_lane + (grp ? C::TP1 : C::TP0);
         uint32_t s_cnt = 0, p_cnt = 0, item_cnt = 0;
         bool ok = true;
 
@@ -298,7 +304,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // S row -> registers: all loads in flight, one wait
                 uint32_t sr[BN];
 #pragma unroll
-                for (int c = 0; c < BN; c += 32) tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(sr + c));
+                for (int c = 0; c < BN; c += 16) tmem_ld16(tS + c, *reinterpret_cast<uint32_t(*)[16]>(sr + c));
                 tmem_wait_ld();
                 reg_fence(sr);
                 tc_fence_before();
@@ -348,13 +354,9 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
                 l_run = l_run * alpha + (a0 + a1);
 
-                // the shared P region is free once the previous P.V product finished; that also
-                // means this tile's O holds every earlier P.V product
-                if (grp == 0) {
-                    if (p_cnt > 0 && !(ok = wait_warp(bars.pv_done[1], (p_cnt - 1) & 1))) break;
-                } else {
-                    if (!(ok = wait_warp(bars.pv_done[0], p_cnt & 1))) break;
-                }
+                // this tile's P region is free, and its O holds every earlier P.V product, once
+                // the previous P.V of this tile has completed
+                if (p_cnt > 0 && !(ok = wait_warp(bars.pv_done[grp], (p_cnt - 1) & 1))) break;
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, rescale)) {
                     const float a = rescale ? alpha : 1.f;
@@ -370,19 +372,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
 #pragma unroll
-                for (int c = 0; c + 32 <= BN / 2; c += 32) {
-                    uint32_t r[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = pk[c + e];
-                    tmem_st32(tP + c, r);
-                }
-                if constexpr ((BN / 2) % 32 != 0) {
-                    constexpr int c = (BN / 2) / 32 * 32;
-                    uint32_t r[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) r[e] = pk[c + e];
-                    tmem_st16(tP + c, r);
-                }
+                for (int c = 0; c < BN / 2; c += 8) tmem_st8(tP + c, *reinterpret_cast<const uint32_t(*)[8]>(pk + c));
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
