@@ -166,20 +166,21 @@ def e2e_step(vit, w, host, device, stream):
 
 
 def load_traffic(kernel: str, workload: str):
-    """dram read+write bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    """dram read+write bytes per launch of `kernel` on `workload`, from the committed ncu summary
+    (profiles/traffic.json), or None when there is none or the kernel source changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(kernel, {})
-    src = e.get("source")
-    if not src or e.get("workload") != workload:
-        return None
-    with open(os.path.join(ROOT, src), "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest()[:16] != e.get("source_sha256_16"):
-            return None
-    return e.get("bytes_per_launch")
+    for e in d.get(kernel, []):
+        if e.get("workload") != workload or not e.get("source"):
+            continue
+        with open(os.path.join(ROOT, e["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != e.get("source_sha256_16"):
+                return None
+        return e.get("bytes_per_launch")
+    return None
 
 
 def kernel_algorithmic_flops(w: wl.Workload, kernel: str, short_max: int) -> float:
