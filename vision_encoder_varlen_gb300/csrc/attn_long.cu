@@ -312,6 +312,9 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (lane == 0) mbar_arrive(bar_addr(bars.s_free[grp]));
                 ++s_cnt;
 
+                // the previous P.V of this tile has almost always finished by now: probe it
+                // without blocking, so its barrier latency overlaps the arithmetic below
+                const bool pv_probe = p_cnt == 0 || mbar_test(bar_addr(bars.pv_done[grp]), (p_cnt - 1) & 1);
                 const int kv_valid = seg_len - j * BN;         // keys of this tile inside the segment
                 if (kv_valid < BN) {
 #pragma unroll
@@ -356,7 +359,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
                 // this tile's P region is free, and its O holds every earlier P.V product, once
                 // the previous P.V of this tile has completed
-                if (p_cnt > 0 && !(ok = wait_warp(bars.pv_done[grp], (p_cnt - 1) & 1))) break;
+                if (!__all_sync(0xffffffffu, pv_probe) && !(ok = wait_warp(bars.pv_done[grp], (p_cnt - 1) & 1))) break;
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, rescale)) {
                     const float a = rescale ? alpha : 1.f;
