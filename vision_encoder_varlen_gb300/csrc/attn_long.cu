@@ -55,14 +55,17 @@ template <int D> struct LongCfg {
     // keys per tile: the largest multiple of 16 (at most 128) with S0, S1 (BN columns each),
     // O0, O1 (D each) and separate P0, P1 (BN/2 each) inside the 512 TMEM columns
     static constexpr int BN = ((512 - 2 * D) / 3 / 16 * 16 > 128) ? 128 : (512 - 2 * D) / 3 / 16 * 16;
+    // K/V ring of 3 slots; the next item's Q pair is prefetched into a second Q buffer
+    // where that still fits in shared memory (all head dims but 128)
     static constexpr int STAGES = 3;
+    static constexpr int QBUF = (4 * (D / 16) * BM * 32 + 3 * 2 * (D / 16) * BN * 32 + 1024 <= 231 * 1024) ? 2 : 1;
     static constexpr int NSLAB = D / 16;
     static constexpr int Q_SLAB = BM * 32;                 // bytes of one 16-column slab of a Q tile
     static constexpr int KV_SLAB = BN * 32;
     static constexpr int Q_TILE = NSLAB * Q_SLAB;
     static constexpr int KV_TILE = NSLAB * KV_SLAB;
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
+    static constexpr int OFF_Q = 0;                        // QBUF buffers x two tiles
+    static constexpr int OFF_K = OFF_Q + QBUF * 2 * Q_TILE;
     static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
     static constexpr int DATA = OFF_V + STAGES * KV_TILE;
     // > half of the SM's shared memory: exactly one CTA (one TMEM owner) per SM
@@ -77,7 +80,7 @@ template <int D> struct LongCfg {
 };
 
 struct Bars {
-    uint64_t q_full, q_empty;
+    uint64_t q_full[2], q_empty[2];
     uint64_t k_full[3], v_full[3], kv_empty[3];
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
     uint64_t drain[2];
@@ -105,8 +108,10 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (threadIdx.x == 0) {
         s_abort = 0;
-        mbar_init(bar_addr(bars.q_full), 1);
-        mbar_init(bar_addr(bars.q_empty), 2);            // one commit from each MMA issuer
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_addr(bars.q_full[b]), 1);
+            mbar_init(bar_addr(bars.q_empty[b]), 2);     // one commit from each MMA issuer
+        }
         for (int s = 0; s < ST; ++s) {
             mbar_init(bar_addr(bars.k_full[s]), 1);
             mbar_init(bar_addr(bars.v_full[s]), 1);
@@ -159,19 +164,22 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             uint32_t g = 0, q_it = 0;
             // parity + 1 of the last load issued on each barrier (0 = none), for the abort drain;
             // two bits per stage, kept in registers
-            uint32_t q_pend = 0, k_pend = 0, v_pend = 0;
+            uint32_t q_pend = 0, k_pend = 0, v_pend = 0;     // q_pend: two bits per Q buffer
             bool ok = true;
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++q_it) {
                 const Item item = items[it];
                 const int seg0 = item.x, seg_len = item.y, q0 = item.z, head = item.w;
                 const int n_kv = (seg_len + BN - 1) / BN;
-                if (q_it > 0 && !(ok = wait(bars.q_empty, (q_it - 1) & 1))) break;
-                mbar_arrive_expect_tx(bar_addr(bars.q_full), 2 * C::Q_TILE);
+                // Q pairs alternate between two buffers, so the next item's Q is loaded while
+                // the current item still runs
+                const uint32_t qb = q_it % C::QBUF, qn = q_it / C::QBUF;   // buffer, its use count
+                if (qn > 0 && !(ok = wait(bars.q_empty[qb], (qn - 1) & 1))) break;
+                mbar_arrive_expect_tx(bar_addr(bars.q_full[qb]), 2 * C::Q_TILE);
                 for (int i = 0; i < 2; ++i)
                     for (int s = 0; s < NSLAB; ++s)
-                        tma_load_2d(smem_addr(base + C::OFF_Q + i * C::Q_TILE + s * C::Q_SLAB), &tm_q,
-                                    head * D + 16 * s, q0 + BM * i, bar_addr(bars.q_full));
-                q_pend = (q_it & 1) + 1;
+                        tma_load_2d(smem_addr(base + C::OFF_Q + (2 * qb + i) * C::Q_TILE + s * C::Q_SLAB), &tm_q,
+                                    head * D + 16 * s, q0 + BM * i, bar_addr(bars.q_full[qb]));
+                q_pend = (q_pend & ~(3u << (2 * qb))) | (((qn & 1) + 1) << (2 * qb));
                 for (int j = 0; j < n_kv; ++j, ++g) {
                     const int st = g % ST;
                     if (g >= (uint32_t)ST && !(ok = wait(bars.kv_empty[st], (g / ST - 1) & 1))) break;
@@ -193,7 +201,11 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // let every copy already issued land before this CTA's shared memory is released
                 // (loads that completed earlier return at once; short budget, abort flag ignored)
                 const int never = 0;
-                if (q_pend) mbar_wait(bar_addr(bars.q_full), q_pend - 1, &never, 20000000ll);
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const uint32_t qp = (q_pend >> (2 * b)) & 3u;
+                    if (qp) mbar_wait(bar_addr(bars.q_full[b]), qp - 1, &never, 20000000ll);
+                }
 #pragma unroll
                 for (int s = 0; s < ST; ++s) {
                     const uint32_t kp = (k_pend >> (2 * s)) & 3u, vp = (v_pend >> (2 * s)) & 3u;
@@ -220,7 +232,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint32_t tS = tmem + (ti ? C::TS1 : C::TS0);
             const uint32_t tO = tmem + (ti ? C::TO1 : C::TO0);
             const uint32_t tP = tmem + (ti ? C::TP1 : C::TP0);
-            const uint64_t dq = smem_desc(smem_addr(base + C::OFF_Q + ti * C::Q_TILE), 16, 256, 6);
+            const uint64_t dq_base = smem_desc(smem_addr(base + C::OFF_Q + ti * C::Q_TILE), 16, 256, 6);
             const uint64_t dk0 = smem_desc(smem_addr(base + C::OFF_K), 16, 256, 6);
             const uint64_t dv0 = smem_desc(smem_addr(base + C::OFF_V), C::KV_SLAB, 256, 6);
             const uint64_t &b_sfree = bars.s_free[ti], &b_pfull = bars.p_full[ti], &b_ofree = bars.o_free[ti];
@@ -228,7 +240,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             uint32_t t = 0, item_cnt = 0;             // global key-tile counter, items done
             bool ok = true;
 
-            auto qk = [&](uint64_t dk) {
+            auto qk = [&](uint64_t dq, uint64_t dk) {
 #pragma unroll
                 for (int kk = 0; kk < NSLAB; ++kk)
                     mma_ss(tS, dq + (uint64_t)(kk * (C::Q_SLAB >> 4)), dk + (uint64_t)(kk * (C::KV_SLAB >> 4)), ID_QK,
@@ -246,13 +258,15 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const Item item = items[it];
                 const int n_kv = (item.y + BN - 1) / BN;
                 uint32_t st = t % ST, ph = (t / ST) & 1;
-                if (!(ok = wait(bars.q_full, item_cnt & 1))) break;
+                const uint32_t qb = item_cnt % C::QBUF;         // Q buffer of this item
+                const uint64_t dq = dq_base + qb * ((2 * C::Q_TILE) >> 4);
+                if (!(ok = wait(bars.q_full[qb], (item_cnt / C::QBUF) & 1))) break;
                 // prologue: S of the item's first key tile
                 if (!(ok = wait(bars.k_full[st], ph))) break;
                 if (t > 0 && !(ok = wait(b_sfree, (t - 1) & 1))) break;
                 tc_fence_after();
-                qk(dk0 + st * STAGE_STEP);
-                if (n_kv == 1) mma_commit(bar_addr(bars.q_empty));
+                qk(dq, dk0 + st * STAGE_STEP);
+                if (n_kv == 1) mma_commit(bar_addr(bars.q_empty[qb]));
                 for (int j = 0; j < n_kv; ++j) {
                     const uint32_t u = t + j;                 // global index of this key tile
                     const uint32_t st1 = (st + 1 == (uint32_t)ST) ? 0u : st + 1;
@@ -261,8 +275,8 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         if (!(ok = wait(bars.k_full[st1], ph1))) break;
                         if (!(ok = wait(b_sfree, u & 1))) break;
                         tc_fence_after();
-                        qk(dk0 + st1 * STAGE_STEP);
-                        if (j + 2 == n_kv) mma_commit(bar_addr(bars.q_empty));
+                        qk(dq, dk0 + st1 * STAGE_STEP);
+                        if (j + 2 == n_kv) mma_commit(bar_addr(bars.q_empty[qb]));
                     }
                     if (!(ok = wait(bars.v_full[st], ph))) break;
                     if (j == 0 && item_cnt > 0 && !(ok = wait(b_ofree, (item_cnt - 1) & 1))) break;

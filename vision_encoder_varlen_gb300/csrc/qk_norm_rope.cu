@@ -10,10 +10,12 @@
 //
 // Layout of the work: a block takes 8 tokens at a time, builds their D/2
 // cos/sin values once in shared memory (shared by all heads and by q and k),
-// then 8-lane groups each own one (token, head, q-or-k) row; lane c holds the
+// then 8-lane groups each own (token, head, q-or-k) rows; lane c holds the
 // 16-byte chunk c of the first half and the matching chunk of the second half,
 // so every rotation pair lives in one thread and the RMS reduction is a
-// three-step shuffle inside the group. HBM-bound: 8*T*H*D bytes move in total.
+// three-step shuffle inside the group. Each group issues the loads of four rows
+// before it computes on any of them, to keep enough bytes in flight.
+// HBM-bound: 8*T*H*D bytes move in total.
 #include "internal.h"
 
 namespace vit {
@@ -21,6 +23,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kTokensPerIter = 8;
+constexpr int kRowBatch = 4;                           // rows per group whose loads are in flight together
 constexpr int kGroup = 8;                              // lanes per row
 constexpr int kGroupsPerBlock = kThreads / kGroup;     // 32
 
@@ -78,61 +81,71 @@ qk_norm_rope_kernel(const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out,
         __syncthreads();
 
         const int nrows = ntok * rows_per_tok;
-        const int nrows_pad = (nrows + kGroupsPerBlock - 1) / kGroupsPerBlock * kGroupsPerBlock;
-        for (int r = grp; r < nrows_pad; r += kGroupsPerBlock) {    // same trip count for every group
-            const bool row_ok = r < nrows;
-            const int tt = row_ok ? r / rows_per_tok : 0;
-            const int rem = row_ok ? r % rows_per_tok : 0;
-            const int which = rem >= H;                 // 0 = q, 1 = k
-            const int h = rem - which * H;
-            const int64_t t = t0 + tt;
-            const bool active = row_ok && c < CHUNKS;
-
-            const __nv_bfloat16 *src = which ? k_in + t * k_in_stride : q_in + t * q_in_stride;
-            __nv_bfloat16 *dst = which ? k_out + t * k_out_stride : q_out + t * q_out_stride;
-            src += (int64_t)h * D + c * 8;
-            dst += (int64_t)h * D + c * 8;
-
-            float xa[8], xb[8];
-            if (active) {
-                unpack8(*reinterpret_cast<const uint4 *>(src), xa);
-                unpack8(*reinterpret_cast<const uint4 *>(src + HALF), xb);
-            } else {
+        constexpr int STEP = kGroupsPerBlock * kRowBatch;
+        const int nrows_pad = (nrows + STEP - 1) / STEP * STEP;
+        for (int r0 = 0; r0 < nrows_pad; r0 += STEP) {            // same trip count for every group
+            uint4 va[kRowBatch], vb[kRowBatch];
+            __nv_bfloat16 *dst[kRowBatch];
+            int tt_[kRowBatch], which_[kRowBatch];
+            bool act[kRowBatch];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) xa[i] = xb[i] = 0.f;
+            for (int k = 0; k < kRowBatch; ++k) {
+                const int r = r0 + k * kGroupsPerBlock + grp;
+                const bool row_ok = r < nrows;
+                const int tt = row_ok ? r / rows_per_tok : 0;
+                const int rem = row_ok ? r % rows_per_tok : 0;
+                const int which = rem >= H;             // 0 = q, 1 = k
+                const int h = rem - which * H;
+                const int64_t t = t0 + tt;
+                act[k] = row_ok && c < CHUNKS;
+                tt_[k] = tt;
+                which_[k] = which;
+                const __nv_bfloat16 *src = (which ? k_in + t * k_in_stride : q_in + t * q_in_stride) + (int64_t)h * D + c * 8;
+                dst[k] = (which ? k_out + t * k_out_stride : q_out + t * q_out_stride) + (int64_t)h * D + c * 8;
+                if (act[k]) {
+                    va[k] = *reinterpret_cast<const uint4 *>(src);
+                    vb[k] = *reinterpret_cast<const uint4 *>(src + HALF);
+                } else {
+                    va[k] = vb[k] = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
-
-            if (use_norm) {
-                float ss = 0.f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) ss = fmaf(xa[i], xa[i], fmaf(xb[i], xb[i], ss));
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-                ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-                const float inv = rsqrtf(ss / (float)D + eps);
-                const float *w = s_w[which];
+            for (int k = 0; k < kRowBatch; ++k) {
+                float xa[8], xb[8];
+                unpack8(va[k], xa);
+                unpack8(vb[k], xb);
+                if (use_norm) {
+                    float ss = 0.f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int m = c * 8 + i;
-                    if (active) {
-                        xa[i] = round_bf16(round_bf16(xa[i] * inv) * w[m]);
-                        xb[i] = round_bf16(round_bf16(xb[i] * inv) * w[m + HALF]);
+                    for (int i = 0; i < 8; ++i) ss = fmaf(xa[i], xa[i], fmaf(xb[i], xb[i], ss));
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+                    const float inv = rsqrtf(ss / (float)D + eps);
+                    const float *w = s_w[which_[k]];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int m = c * 8 + i;
+                        if (act[k]) {
+                            xa[i] = round_bf16(round_bf16(xa[i] * inv) * w[m]);
+                            xb[i] = round_bf16(round_bf16(xb[i] * inv) * w[m + HALF]);
+                        }
                     }
                 }
-            }
-
-            if (active) {
-                uint32_t oa[4], ob[4];
+                if (act[k]) {
+                    const float *cs_ = s_cos[tt_[k]], *sn_ = s_sin[tt_[k]];
+                    uint32_t oa[4], ob[4];
 #pragma unroll
-                for (int i = 0; i < 8; i += 2) {
-                    const int m = c * 8 + i;
-                    const float c0 = s_cos[tt][m], s0 = s_sin[tt][m];
-                    const float c1 = s_cos[tt][m + 1], s1 = s_sin[tt][m + 1];
-                    oa[i / 2] = pack2(xa[i] * c0 - xb[i] * s0, xa[i + 1] * c1 - xb[i + 1] * s1);
-                    ob[i / 2] = pack2(xb[i] * c0 + xa[i] * s0, xb[i + 1] * c1 + xa[i + 1] * s1);
+                    for (int i = 0; i < 8; i += 2) {
+                        const int m = c * 8 + i;
+                        const float c0 = cs_[m], s0 = sn_[m];
+                        const float c1 = cs_[m + 1], s1 = sn_[m + 1];
+                        oa[i / 2] = pack2(xa[i] * c0 - xb[i] * s0, xa[i + 1] * c1 - xb[i + 1] * s1);
+                        ob[i / 2] = pack2(xb[i] * c0 + xa[i] * s0, xb[i + 1] * c1 + xa[i + 1] * s1);
+                    }
+                    *reinterpret_cast<uint4 *>(dst[k]) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+                    *reinterpret_cast<uint4 *>(dst[k] + HALF) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
                 }
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-                *reinterpret_cast<uint4 *>(dst + HALF) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
             }
         }
     }
