@@ -318,9 +318,9 @@ def run_ours(args, rank, world, local):
     if dom is not None:
         n, tot = kt[dom]
         avg_s = tot / n * 1e-3
-        if dom.startswith("attn"):
-            short_max = vit.set_short_segment_max(128)
-            vit.set_short_segment_max(short_max)
+        short_max = vit.set_short_segment_max(128)
+        vit.set_short_segment_max(short_max)
+        if dom == "attn_long":
             alg = kernel_algorithmic_flops(w, dom, short_max)
             peak = peaks["bf16_tflops_sustained"]
             achieved = alg / avg_s / 1e12
@@ -329,11 +329,17 @@ def run_ours(args, rank, world, local):
                         "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside a long step loop)",
                         "algorithmic_flops_per_launch": alg}
         else:
-            alg = 8.0 * T * H * D if dom == "qk_norm_rope" else 8.0 * T
+            if dom == "attn_short":      # q, k, v read and out written once per token it owns
+                L = w.lengths
+                alg = 8.0 * float(L[L <= short_max].sum()) * H * D
+            elif dom == "qk_norm_rope":  # q and k read and written once
+                alg = 8.0 * T * H * D
+            else:
+                alg = 8.0 * T
             achieved = alg / avg_s / 1e9
             roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(dom, w.name),
-                        "peak_source": f"{peaks_src} hbm_gbs"}
+                        "peak_source": f"{peaks_src} hbm_gbs", "algorithmic_bytes_per_launch": alg}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -398,8 +404,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5, 6],
-                    help="workload 1..5 (default 5); 6 = a single 128x128 image for profiler captures")
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5, 6, 7],
+                    help="workload 1..5 (default 5); 6 = a single 128x128 image for profiler captures; "
+                         "7 = 2048 small images for the short-segment kernel")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

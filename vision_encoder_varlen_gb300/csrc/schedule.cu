@@ -141,7 +141,9 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, int B, int64_t T, int H,
         run += (int64_t)H * ((len + bm - 1) / bm);
     }
     __syncthreads();
-    for (int p = 0; p < B; ++p) {
+    // one warp per sorted segment (a whole-block loop over B segments would leave most threads idle)
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int p = warp; p < B; p += kThreads / 32) {
         const int seg = (int)(s_key[p] & 0xffffffffu);
         const int len = s_len[seg];
         if (len == 0) continue;
@@ -149,7 +151,7 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, int B, int64_t T, int H,
         const int nq = (len + bm - 1) / bm;
         const int start = s_start[seg];
         Item *dst = items + s_off[p];
-        for (int i = tid; i < H * nq; i += kThreads) {
+        for (int i = lane; i < H * nq; i += 32) {
             const int h = i / nq, qb = i - h * nq;
             dst[i] = make_int4(start, len, start + qb * bm, h);
         }
