@@ -229,6 +229,8 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
+    if args.short_max is not None:
+        vit.set_short_segment_max(args.short_max)
     w = wl.make_config(args.config)
     t = w.tensors()
     T, H, D = w.total_tokens, w.heads, w.head_dim
@@ -406,11 +408,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5, 6, 7],
                     help="workload 1..5 (default 5); 6 = a single 128x128 image for profiler captures; "
-                         "7 = 2048 small images for the short-segment kernel")
+                         "7 = 4096 small images for the short-segment kernel")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--short-max", type=int, default=None,
+                    help="segments longer than this run on the tcgen05 kernel (library default 64)")
     ap.add_argument("--ref-rows", type=int, default=16)
     args = ap.parse_args()
     if args.warmup < 3:

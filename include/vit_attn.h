@@ -206,7 +206,8 @@ vit_status_t vit_varlen_attn_noalloc(const void *q, const void *k, const void *v
 /*
  * Kernel split of vit_varlen_attn: segments longer than `short_max` tokens run
  * on the tcgen05/TMEM long-segment kernel (256 query rows per work item), the
- * others on the short-segment kernel (64 query rows per item). Default 128.
+ * others on the short-segment kernel (128 query rows per item). Default 64, the
+ * measured crossover of the two kernels on GB300.
  * 0 sends every segment to the long kernel, INT_MAX every segment to the short
  * one; the results agree within the output tolerance either way. Process-wide
  * setting read at each call; returns the previous value.

@@ -20,7 +20,7 @@ def _built():
     _build.build()
 
 
-SPLITS = {"default": 128, "all_long": 0, "all_short": 2 ** 31 - 1}
+SPLITS = {"default": 64, "all_long": 0, "all_short": 2 ** 31 - 1}
 
 
 @pytest.fixture(params=list(SPLITS))

@@ -188,7 +188,7 @@ def varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: t
 
 
 def set_short_segment_max(short_max: int) -> int:
-    """Segments longer than short_max go to the tcgen05 long-segment kernel (default 128).
+    """Segments longer than short_max go to the tcgen05 long-segment kernel (default 64).
     Returns the previous value."""
     return int(lib().vit_set_short_segment_max(int(short_max)))
 

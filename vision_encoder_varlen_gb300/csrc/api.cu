@@ -54,7 +54,9 @@ vit_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? VIT_OK : VIT_E
 constexpr int64_t kMaxTokens = (int64_t)1 << 31;
 
 // Segments longer than this run on the tcgen05 long-segment kernel.
-std::atomic<int> g_short_max{128};
+// Measured crossover on GB300: the warp-MMA kernel wins below ~32 tokens, the two tie at
+// 32-64, the tcgen05 kernel wins from 64 tokens up (30 % at 64-128, 3x beyond).
+std::atomic<int> g_short_max{64};
 // Test hook: when set, the long-segment kernel never loads V, so its bounded waits expire.
 std::atomic<int> g_stall_v{0};
 
@@ -139,7 +141,9 @@ vit_status_t vit_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, v
 size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D)
 {
     if (T < 0 || T >= kMaxTokens || H < 1 || B < 0 || B > VIT_MAX_SEGMENTS || !head_dim_ok(D)) return 0;
-    const int64_t items = max_items(T, H, B, attn_short_bm());
+    // every work item covers at least 64 query rows (128 for short segments, 256 for long
+    // ones), so this bound holds for any kernel split
+    const int64_t items = max_items(T, H, B, 64);
     return sizeof(WsHeader) + sizeof(Item) * (size_t)items;
 }
 

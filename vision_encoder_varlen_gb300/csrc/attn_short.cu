@@ -1,6 +1,6 @@
-// Short-segment varlen attention: 64-query-row tiles on warp-level MMA.
+// Short-segment varlen attention on warp-level MMA.
 //
-// Computes, for each work item (segment, head, 64-row query block) of the
+// Computes, for each work item (segment, head, 128-row query block) of the
 // scheduler's list, out = softmax(scale * q k^T) v over the keys of that
 // segment only (vLLM Dots vision_attention page, VisionAttentionV2.forward:
 // plain attention per segment; VisionAttention.forward: the same result
@@ -8,11 +8,21 @@
 // float32) on the same page), probabilities rounded to bf16 for the P.V
 // product, fp32 accumulation, bf16 output.
 //
-// Segments up to a few hundred tokens are HBM/latency bound (arithmetic
-// intensity ~L/2 flop/byte), so this path favours many small independent
-// CTAs: 4 warps x 16 query rows, 64-key tiles double-buffered with cp.async,
-// online softmax in registers (exp2 with the scale folded in), and rows
-// outside the segment zero-filled on load so no other segment is ever read.
+// Segments of up to ~128 tokens are HBM-bound (arithmetic intensity ~L/2
+// flop/byte), so the design aims at touching every byte once and wasting
+// little arithmetic on padding:
+//   - one item covers 128 query rows, so a segment of <= 128 tokens is one
+//     item per head and its K and V are read from HBM exactly once;
+//   - 4 warps, each owning 32 query rows as two 16-row MMA tiles that share
+//     every K and V fragment loaded from shared memory;
+//   - keys in 64-key sub-chunks with an online softmax; 16-key groups past the
+//     segment end and 16-row tiles past it are skipped, so padding costs at
+//     most 15 rows and 15 keys;
+//   - rows outside the segment are zero-filled on load and never read from
+//     HBM, so no other segment is ever touched; several CTAs per SM overlap
+//     one item's loads with another's arithmetic.
+// Any segment length works (longer ones loop over 128-key tiles); the
+// long-segment kernel normally takes those.
 #include "internal.h"
 
 namespace vit {
@@ -20,14 +30,15 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int BM = 64;   // query rows per item (16 per warp)
-constexpr int BN = 64;   // keys per tile
+constexpr int BM = 128;   // query rows per item (32 per warp = two 16-row tiles)
+constexpr int BN = 128;   // keys per shared-memory tile
+constexpr int SUB = 64;   // keys per softmax sub-chunk
 
 template <int D> struct ShortCfg {
     static constexpr int PITCH = D + 8;                          // smem row pitch (elements): conflict-free ldmatrix
-    static constexpr int Q_ELEMS = BM * PITCH;
-    static constexpr int KV_ELEMS = BN * PITCH;
-    static constexpr size_t SMEM = sizeof(__nv_bfloat16) * (Q_ELEMS + 4 * KV_ELEMS);
+    static constexpr int ELEMS = 128 * PITCH;                    // one 128-row tile
+    static constexpr size_t SMEM = sizeof(__nv_bfloat16) * 3 * ELEMS;   // Q, K, V
+    static constexpr int MIN_BLOCKS = D <= 32 ? 3 : 2;          // CTAs per SM the register budget allows
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -39,9 +50,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool v
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N> __device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -52,13 +61,12 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 
-__device__ __forceinline__ void mma16816(float *c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                         uint32_t b1) {
+__device__ __forceinline__ void mma16816(float *c, const uint32_t *a, uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};\n"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -72,10 +80,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Copy `rows` rows of D bf16 (row r of the tile = token row0 + r) into smem with
-// the padded pitch; rows >= valid_rows are zero-filled and never read from HBM.
+// Copy rows [0, rows) of a tile (row r = token row0 + r) into smem with the padded
+// pitch; rows >= valid_rows are zero-filled and never read from HBM.
 template <int D>
-__device__ __forceinline__ void load_tile(__nv_bfloat16 *s, const __nv_bfloat16 *g, int64_t stride, int64_t row0,
+__device__ __forceinline__ void load_rows(__nv_bfloat16 *s, const __nv_bfloat16 *g, int64_t stride, int64_t row0,
                                           int rows, int valid_rows) {
     constexpr int CH = D / 8;                                    // 16-byte chunks per row
     for (int i = threadIdx.x; i < rows * CH; i += kThreads) {
@@ -87,7 +95,7 @@ __device__ __forceinline__ void load_tile(__nv_bfloat16 *s, const __nv_bfloat16 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, ShortCfg<D>::MIN_BLOCKS)
 attn_short_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                   const __nv_bfloat16 *__restrict__ v, int64_t q_stride, int64_t k_stride, int64_t v_stride,
                   __nv_bfloat16 *__restrict__ out, int64_t out_stride, float scale_log2,
@@ -99,12 +107,13 @@ attn_short_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
     constexpr int DN = D / 8;            // output n-blocks of 8 columns
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
-    __nv_bfloat16 *sK = sQ + C::Q_ELEMS;                     // [2][BN][PITCH]
-    __nv_bfloat16 *sV = sK + 2 * C::KV_ELEMS;                // [2][BN][PITCH]
+    __nv_bfloat16 *sK = sQ + C::ELEMS;
+    __nv_bfloat16 *sV = sK + C::ELEMS;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tig = lane & 3;
     const int n_items = hdr->n_short, first = hdr->n_long;
+    const int r_base = warp * 32;
 
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const Item item = items[first + it];
@@ -113,137 +122,163 @@ attn_short_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
         const int q_valid = min(BM, seg_end - q0);
         const int n_tiles = (seg_len + BN - 1) / BN;
         const __nv_bfloat16 *qh = q + head * D, *kh = k + head * D, *vh = v + head * D;
+        // 16-row tiles of this warp that hold at least one query row of the segment
+        const bool act0 = r_base < q_valid, act1 = r_base + 16 < q_valid;
 
         __syncthreads();                                     // smem of the previous item is free
-        load_tile<D>(sQ, qh, q_stride, q0, BM, q_valid);
-        load_tile<D>(sK, kh, k_stride, seg0, BN, min(BN, seg_len));
-        load_tile<D>(sV, vh, v_stride, seg0, BN, min(BN, seg_len));
-        cp_async_commit();
+        load_rows<D>(sQ, qh, q_stride, q0, (q_valid + 15) & ~15, q_valid);
 
-        float o[DN][4];
+        float o[2][DN][4];
 #pragma unroll
-        for (int i = 0; i < DN; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
-        uint32_t qf[KSTEPS][4];
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int i = 0; i < DN; ++i) o[mt][i][0] = o[mt][i][1] = o[mt][i][2] = o[mt][i][3] = 0.f;
+        float m_r[2][2] = {{-INFINITY, -INFINITY}, {-INFINITY, -INFINITY}};
+        float l_r[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 
         for (int j = 0; j < n_tiles; ++j) {
-            const int st = j & 1;
-            if (j + 1 < n_tiles) {
-                const int kv0 = seg0 + (j + 1) * BN;
-                const int valid = min(BN, seg_end - kv0);
-                load_tile<D>(sK + (st ^ 1) * C::KV_ELEMS, kh, k_stride, kv0, BN, valid);
-                load_tile<D>(sV + (st ^ 1) * C::KV_ELEMS, vh, v_stride, kv0, BN, valid);
-                cp_async_commit();
-                cp_async_wait<1>();
-            } else {
-                cp_async_wait<0>();
-            }
+            const int kv0 = seg0 + j * BN;
+            const int kv_valid = min(BN, seg_end - kv0);
+            if (j > 0) __syncthreads();                      // every warp is done with the previous K/V tile
+            load_rows<D>(sK, kh, k_stride, kv0, (kv_valid + 15) & ~15, kv_valid);
+            load_rows<D>(sV, vh, v_stride, kv0, (kv_valid + 15) & ~15, kv_valid);
+            cp_async_commit();
+            cp_async_wait_all();
             __syncthreads();
+            if (!act0) continue;                             // warp-uniform: nothing of the segment in its rows
 
-            if (j == 0) {
+            for (int sc = 0; sc * SUB < kv_valid; ++sc) {
+                const int k0 = sc * SUB;
+                const int nvalid = min(SUB, kv_valid - k0);  // valid keys of this sub-chunk
+                const int npairs = (nvalid + 15) >> 4;       // 16-key groups that hold a valid key
+
+                // S = Q K^T for 32 rows x 64 keys (skipping empty 16-key groups / row tiles)
+                float s[2][SUB / 8][4];
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int nb = 0; nb < SUB / 8; ++nb) s[mt][nb][0] = s[mt][nb][1] = s[mt][nb][2] = s[mt][nb][3] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
-                    const int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    uint32_t a[2][4];
                     const int col = kk * 16 + (lane >> 4) * 8;
-                    ldsm_x4(smem_u32(sQ + row * PITCH + col), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+                    const int row = r_base + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    ldsm_x4(smem_u32(sQ + row * PITCH + col), a[0][0], a[0][1], a[0][2], a[0][3]);
+                    if (act1) ldsm_x4(smem_u32(sQ + (row + 16) * PITCH + col), a[1][0], a[1][1], a[1][2], a[1][3]);
+#pragma unroll
+                    for (int np = 0; np < SUB / 16; ++np) {
+                        if (np < npairs) {
+                            const int n = k0 + np * 16 + (lane & 7) + (lane >> 4) * 8;
+                            const int kc = kk * 16 + ((lane >> 3) & 1) * 8;
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(smem_u32(sK + n * PITCH + kc), b0, b1, b2, b3);
+                            mma16816(s[0][2 * np], a[0], b0, b1);
+                            mma16816(s[0][2 * np + 1], a[0], b2, b3);
+                            if (act1) {
+                                mma16816(s[1][2 * np], a[1], b0, b1);
+                                mma16816(s[1][2 * np + 1], a[1], b2, b3);
+                            }
+                        }
+                    }
                 }
-            }
 
-            // S = Q K^T for this warp's 16 rows x 64 keys
-            const __nv_bfloat16 *sKs = sK + st * C::KV_ELEMS;
-            float s[BN / 8][4];
+                // online softmax in the log2 domain; keys past the segment end -> -inf
 #pragma unroll
-            for (int nb = 0; nb < BN / 8; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
+                for (int mt = 0; mt < 2; ++mt) {
+                    if (mt == 1 && !act1) break;             // warp-uniform
+                    float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
+                    for (int nb = 0; nb < SUB / 8; ++nb) {
 #pragma unroll
-                for (int nb = 0; nb < BN / 8; nb += 2) {
-                    const int n = nb * 8 + (lane & 7) + (lane >> 4) * 8;
-                    const int kc = kk * 16 + ((lane >> 3) & 1) * 8;
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(smem_u32(sKs + n * PITCH + kc), b0, b1, b2, b3);
-                    mma16816(s[nb], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-                    mma16816(s[nb + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = nb * 8 + tig * 2 + (e & 1);
+                            float x = s[mt][nb][e] * scale_log2;
+                            if (c >= nvalid) x = -INFINITY;
+                            s[mt][nb][e] = x;
+                            mx[e >> 1] = fmaxf(mx[e >> 1], x);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                        const float m_new = fmaxf(m_r[mt][r], mx[r]);
+                        const float alpha = ex2(m_r[mt][r] - m_new);
+                        m_r[mt][r] = m_new;
+                        l_r[mt][r] *= alpha;
+#pragma unroll
+                        for (int nd = 0; nd < DN; ++nd) {
+                            o[mt][nd][2 * r] *= alpha;
+                            o[mt][nd][2 * r + 1] *= alpha;
+                        }
+                    }
+#pragma unroll
+                    for (int nb = 0; nb < SUB / 8; ++nb) {
+                        if (nb < 2 * npairs) {                   // groups past the segment end stay 0
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float p = ex2(s[mt][nb][e] - m_r[mt][e >> 1]);
+                                s[mt][nb][e] = p;
+                                l_r[mt][e >> 1] += p;
+                            }
+                        }
+                    }
                 }
-            }
 
-            // scale into the log2 domain, mask keys past the segment end, online softmax
-            const int kv_valid = min(BN, seg_end - (seg0 + j * BN));
-            float mx[2] = {-INFINITY, -INFINITY};
+                // O += P V over the 16-key groups that hold valid keys
 #pragma unroll
-            for (int nb = 0; nb < BN / 8; ++nb) {
+                for (int np = 0; np < SUB / 16; ++np) {
+                    if (np < npairs) {
+                        uint32_t pa[2][4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int col = nb * 8 + tig * 2 + (e & 1);
-                    float x = s[nb][e] * scale_log2;
-                    if (col >= kv_valid) x = -INFINITY;
-                    s[nb][e] = x;
-                    mx[e >> 1] = fmaxf(mx[e >> 1], x);
+                        for (int mt = 0; mt < 2; ++mt) {
+                            pa[mt][0] = pack_bf16(s[mt][2 * np][0], s[mt][2 * np][1]);
+                            pa[mt][1] = pack_bf16(s[mt][2 * np][2], s[mt][2 * np][3]);
+                            pa[mt][2] = pack_bf16(s[mt][2 * np + 1][0], s[mt][2 * np + 1][1]);
+                            pa[mt][3] = pack_bf16(s[mt][2 * np + 1][2], s[mt][2 * np + 1][3]);
+                        }
+                        const int row = k0 + np * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                        for (int nd = 0; nd < DN; nd += 2) {
+                            const int col = nd * 8 + (lane >> 4) * 8;
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4_t(smem_u32(sV + row * PITCH + col), b0, b1, b2, b3);
+                            mma16816(o[0][nd], pa[0], b0, b1);
+                            mma16816(o[0][nd + 1], pa[0], b2, b3);
+                            if (act1) {
+                                mma16816(o[1][nd], pa[1], b0, b1);
+                                mma16816(o[1][nd + 1], pa[1], b2, b3);
+                            }
+                        }
+                    }
                 }
             }
-            float alpha[2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                const float m_new = fmaxf(m_r[r], mx[r]);
-                alpha[r] = ex2(m_r[r] - m_new);
-                m_r[r] = m_new;
-                l_r[r] *= alpha[r];
-            }
-#pragma unroll
-            for (int nb = 0; nb < DN; ++nb) {
-                o[nb][0] *= alpha[0];
-                o[nb][1] *= alpha[0];
-                o[nb][2] *= alpha[1];
-                o[nb][3] *= alpha[1];
-            }
-            uint32_t pf[BN / 16][4];
-#pragma unroll
-            for (int nb = 0; nb < BN / 8; ++nb) {
-                const float p0 = ex2(s[nb][0] - m_r[0]), p1 = ex2(s[nb][1] - m_r[0]);
-                const float p2 = ex2(s[nb][2] - m_r[1]), p3 = ex2(s[nb][3] - m_r[1]);
-                l_r[0] += p0 + p1;
-                l_r[1] += p2 + p3;
-                pf[nb >> 1][(nb & 1) * 2 + 0] = pack_bf16(p0, p1);
-                pf[nb >> 1][(nb & 1) * 2 + 1] = pack_bf16(p2, p3);
-            }
-
-            // O += P V
-            const __nv_bfloat16 *sVs = sV + st * C::KV_ELEMS;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-#pragma unroll
-                for (int nd = 0; nd < DN; nd += 2) {
-                    const int row = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const int col = nd * 8 + (lane >> 4) * 8;
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(smem_u32(sVs + row * PITCH + col), b0, b1, b2, b3);
-                    mma16816(o[nd], pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3], b0, b1);
-                    mma16816(o[nd + 1], pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3], b2, b3);
-                }
-            }
-            __syncthreads();                                 // stage st may be refilled next iteration
         }
 
         // normalise and store the rows that belong to the segment
+        if (act0) {
+            __nv_bfloat16 *oh = out + head * D;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
-            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
-        }
-        const float inv0 = 1.f / l_r[0], inv1 = 1.f / l_r[1];
-        const int r0 = warp * 16 + g, r1 = r0 + 8;
-        __nv_bfloat16 *oh = out + head * D;
+            for (int mt = 0; mt < 2; ++mt) {
+                if (mt == 1 && !act1) break;
 #pragma unroll
-        for (int nd = 0; nd < DN; ++nd) {
-            const int col = nd * 8 + tig * 2;
-            if (r0 < q_valid)
-                *reinterpret_cast<uint32_t *>(oh + (int64_t)(q0 + r0) * out_stride + col) =
-                    pack_bf16(o[nd][0] * inv0, o[nd][1] * inv0);
-            if (r1 < q_valid)
-                *reinterpret_cast<uint32_t *>(oh + (int64_t)(q0 + r1) * out_stride + col) =
-                    pack_bf16(o[nd][2] * inv1, o[nd][3] * inv1);
+                for (int r = 0; r < 2; ++r) {
+                    l_r[mt][r] += __shfl_xor_sync(0xffffffffu, l_r[mt][r], 1);
+                    l_r[mt][r] += __shfl_xor_sync(0xffffffffu, l_r[mt][r], 2);
+                }
+                const float inv0 = 1.f / l_r[mt][0], inv1 = 1.f / l_r[mt][1];
+                const int r0 = r_base + mt * 16 + g, r1 = r0 + 8;
+#pragma unroll
+                for (int nd = 0; nd < DN; ++nd) {
+                    const int col = nd * 8 + tig * 2;
+                    if (r0 < q_valid)
+                        *reinterpret_cast<uint32_t *>(oh + (int64_t)(q0 + r0) * out_stride + col) =
+                            pack_bf16(o[mt][nd][0] * inv0, o[mt][nd][1] * inv0);
+                    if (r1 < q_valid)
+                        *reinterpret_cast<uint32_t *>(oh + (int64_t)(q0 + r1) * out_stride + col) =
+                            pack_bf16(o[mt][nd][2] * inv1, o[mt][nd][3] * inv1);
+                }
+            }
         }
     }
 }

@@ -135,9 +135,9 @@ def make_config(idx: int) -> Workload:
         # (168 MB of q/k/v/out, above the 129 MB L2, ~1.5 ms of attention)
         return Workload("profile_128x128_h16_d80_qknorm", ((128, 128),), 16, 80, True, seed=seed)
     if idx == 7:
-        # not one of the five study shapes: 2048 small images (36..121 tokens) that all run on the
+        # not one of the five study shapes: 4096 small images (16..64 tokens) that all run on the
         # short-segment kernel, for its HBM-bandwidth measurement (~1.5 GB of q/k/v/out)
-        return Workload("short_2048img_6..11_h16_d80_qknorm", _uniform_grids(rng, 2048, 6, 11, 6, 11), 16, 80, True,
+        return Workload("short_4096img_4..8_h16_d80_qknorm", _uniform_grids(rng, 4096, 4, 8, 4, 8), 16, 80, True,
                         seed=seed)
     raise ValueError(f"no workload {idx}")
 
