@@ -364,6 +364,44 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_split_sweep(args):
+    """Attention time with every segment on the warp-MMA kernel vs every segment on the tcgen05
+    kernel, for bands of random segment lengths (one JSON line per band and head_dim)."""
+    import vision_encoder_varlen_gb300 as vit
+    from vision_encoder_varlen_gb300 import _build
+    _build.build()
+    rng = np.random.default_rng(0)
+    prev = vit.set_short_segment_max(64)
+    try:
+        for D in (80, 128):
+            for lo, hi in ((4, 16), (16, 32), (32, 64), (64, 128), (128, 256), (256, 512)):
+                lengths = rng.integers(lo, hi + 1, size=8192 if hi <= 32 else (4096 if hi <= 128 else 2048))
+                w = wl.from_lengths(lengths, 16, D, max_seqlen_meta=4096)
+                g = torch.Generator(device="cuda").manual_seed(1)
+                T = w.total_tokens
+                q, k, v = (torch.randn(T, 16, D, device="cuda", generator=g).to(torch.bfloat16) for _ in range(3))
+                cu = torch.from_numpy(w.cu_seqlens).cuda()
+                ws = torch.empty(vit.workspace_size(T, 16, w.num_segments, D), dtype=torch.uint8, device="cuda")
+                out = torch.empty_like(q)
+                res = {}
+                for name, sm in (("short_kernel_ms", 1 << 30), ("tcgen05_kernel_ms", 0)):
+                    vit.set_short_segment_max(sm)
+                    for _ in range(args.warmup):
+                        vit.varlen_attn(q, k, v, cu, 4096, out=out, workspace=ws)
+                    torch.cuda.synchronize()
+                    vit.kernel_timing_read()
+                    vit.kernel_timing(True)
+                    for _ in range(args.steps):
+                        vit.varlen_attn(q, k, v, cu, 4096, out=out, workspace=ws)
+                    vit.kernel_timing(False)
+                    kt = vit.kernel_timing_read()
+                    res[name] = sum(t for _, t in kt.values()) / args.steps
+                print(json.dumps({"sweep": "split", "head_dim": D, "lengths": [lo, hi], "segments": int(len(lengths)),
+                                  "tokens": T, **res}), flush=True)
+    finally:
+        vit.set_short_segment_max(prev)
+
+
 def run_reference(args, rank, world):
     """The reference arm: the fp64 oracle, as it stands, on the host cores; each
     step is a bounded sample (query rows of the longest image, all heads)."""
@@ -413,6 +451,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--sweep-split", action="store_true",
+                    help="time both attention kernels over bands of segment lengths and exit")
     ap.add_argument("--short-max", type=int, default=None,
                     help="segments longer than this run on the tcgen05 kernel (library default 64)")
     ap.add_argument("--ref-rows", type=int, default=16)
@@ -420,6 +460,9 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
+    if args.sweep_split:
+        run_split_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

@@ -41,8 +41,39 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ float round_bf16(float x) {
-    return __bfloat162float(__float2bfloat16_rn(x));
+// ---- packed pairs: Blackwell f32x2 arithmetic and bf16x2 multiply
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t v;
+    asm("mov.b64 %0, {%1, %2};\n" : "=l"(v) : "f"(lo), "f"(hi));
+    return v;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// bf16(bf16(x0*inv) * w0), bf16(bf16(x1*inv) * w1) as two floats: the product of two bf16
+// values is exact in fp32, so one bf16x2 multiply rounds exactly like the scalar form
+__device__ __forceinline__ void norm_pair(float &x0, float &x1, float inv, uint32_t w2) {
+    const uint32_t t = pack2(x0 * inv, x1 * inv);
+    __nv_bfloat162 y = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&t),
+                               *reinterpret_cast<const __nv_bfloat162 *>(&w2));
+    const uint32_t u = *reinterpret_cast<uint32_t *>(&y);
+    x0 = __uint_as_float(u << 16);
+    x1 = __uint_as_float(u & 0xffff0000u);
 }
 
 template <int D>
@@ -55,28 +86,31 @@ qk_norm_rope_kernel(const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out,
 {
     constexpr int HALF = D / 2, QUART = D / 4, CHUNKS = HALF / 8;
     static_assert(HALF % 8 == 0 && CHUNKS <= kGroup, "head_dim must split into 16-byte chunks");
-    __shared__ float s_cos[kTokensPerIter][HALF];
-    __shared__ float s_sin[kTokensPerIter][HALF];
-    __shared__ float s_w[2][D];
+    // per token and pair (m, m+1): {cos a_m, cos a_m+1, sin a_m, sin a_m+1}, one 16-byte read
+    __shared__ float4 s_cs[kTokensPerIter][HALF / 2];
+    __shared__ __align__(16) uint32_t s_w[2][D / 2];      // bf16x2 weight pairs (q row, k row)
 
     const int tid = threadIdx.x;
     const int grp = tid / kGroup, c = tid % kGroup;
     const bool use_norm = norm_w != nullptr;
     if (use_norm)
-        for (int i = tid; i < 2 * D; i += kThreads) s_w[i / D][i % D] = __bfloat162float(norm_w[i]);
+        for (int i = tid; i < D; i += kThreads)
+            s_w[i / (D / 2)][i % (D / 2)] = reinterpret_cast<const uint32_t *>(norm_w)[i];
 
     const int rows_per_tok = 2 * H;
     for (int64_t t0 = (int64_t)blockIdx.x * kTokensPerIter; t0 < T; t0 += (int64_t)gridDim.x * kTokensPerIter) {
         __syncthreads();                                // previous iteration done with s_cos/s_sin
         const int ntok = (int)(T - t0 < kTokensPerIter ? T - t0 : kTokensPerIter);
-        for (int i = tid; i < ntok * HALF; i += kThreads) {
-            const int tt = i / HALF, m = i % HALF;
+        for (int i = tid; i < ntok * (HALF / 2); i += kThreads) {
+            const int tt = i / (HALF / 2), m = 2 * (i % (HALF / 2));
             const int2 p = pos_hw[t0 + tt];
-            const float ang = (float)(m < QUART ? p.x : p.y) * inv_freq[m < QUART ? m : m - QUART];
-            float sn, cs;
-            sincosf(ang, &sn, &cs);
-            s_cos[tt][m] = cs;
-            s_sin[tt][m] = sn;
+            // m is even and D/4 is even, so m and m + 1 are both row angles or both column angles
+            const float pos = (float)(m < QUART ? p.x : p.y);
+            const int f = m < QUART ? m : m - QUART;
+            float s0, c0, s1, c1;
+            sincosf(pos * inv_freq[f], &s0, &c0);
+            sincosf(pos * inv_freq[f + 1], &s1, &c1);
+            s_cs[tt][m / 2] = make_float4(c0, c1, s0, s1);
         }
         __syncthreads();
 
@@ -122,26 +156,30 @@ qk_norm_rope_kernel(const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out,
                     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
                     ss += __shfl_xor_sync(0xffffffffu, ss, 4);
                     const float inv = rsqrtf(ss / (float)D + eps);
-                    const float *w = s_w[which_[k]];
+                    if (act[k]) {                                // idle lanes (c >= CHUNKS) read nothing
+                        const uint4 wa = *reinterpret_cast<const uint4 *>(&s_w[which_[k]][c * 4]);
+                        const uint4 wb = *reinterpret_cast<const uint4 *>(&s_w[which_[k]][HALF / 2 + c * 4]);
+                        const uint32_t wa_[4] = {wa.x, wa.y, wa.z, wa.w}, wb_[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int m = c * 8 + i;
-                        if (act[k]) {
-                            xa[i] = round_bf16(round_bf16(xa[i] * inv) * w[m]);
-                            xb[i] = round_bf16(round_bf16(xb[i] * inv) * w[m + HALF]);
+                        for (int i = 0; i < 8; i += 2) {
+                            norm_pair(xa[i], xa[i + 1], inv, wa_[i / 2]);
+                            norm_pair(xb[i], xb[i + 1], inv, wb_[i / 2]);
                         }
                     }
                 }
                 if (act[k]) {
-                    const float *cs_ = s_cos[tt_[k]], *sn_ = s_sin[tt_[k]];
+                    const float4 *cs_ = s_cs[tt_[k]] + c * 4;
                     uint32_t oa[4], ob[4];
 #pragma unroll
                     for (int i = 0; i < 8; i += 2) {
-                        const int m = c * 8 + i;
-                        const float c0 = cs_[m], s0 = sn_[m];
-                        const float c1 = cs_[m + 1], s1 = sn_[m + 1];
-                        oa[i / 2] = pack2(xa[i] * c0 - xb[i] * s0, xa[i + 1] * c1 - xb[i + 1] * s1);
-                        ob[i / 2] = pack2(xb[i] * c0 + xa[i] * s0, xb[i + 1] * c1 + xa[i + 1] * s1);
+                        const float4 t = cs_[i / 2];
+                        const uint64_t cc = f2(t.x, t.y), sn = f2(t.z, t.w);
+                        const uint64_t a = f2(xa[i], xa[i + 1]), b = f2(xb[i], xb[i + 1]);
+                        float ya0, ya1, yb0, yb1;
+                        f2_split(f2_sub(f2_mul(a, cc), f2_mul(b, sn)), ya0, ya1);     // x cos - x' sin
+                        f2_split(f2_fma(a, sn, f2_mul(b, cc)), yb0, yb1);             // x' cos + x sin
+                        oa[i / 2] = pack2(ya0, ya1);
+                        ob[i / 2] = pack2(yb0, yb1);
                     }
                     *reinterpret_cast<uint4 *>(dst[k]) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
                     *reinterpret_cast<uint4 *>(dst[k] + HALF) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
