@@ -56,11 +56,11 @@ def _load():
             lib.vo_grid_positions.restype = ctypes.c_int64
             lib.vo_norm_rope.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                          _i32p, ctypes.c_double, ctypes.c_void_p, ctypes.c_int,
-                                         ctypes.c_double, _f64p]
+                                         ctypes.c_double, ctypes.c_int, _f64p]
             lib.vo_norm_rope.restype = None
             lib.vo_attention.argtypes = [_f64p, _f64p, _f64p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                          _i32p, ctypes.c_int, ctypes.c_double, ctypes.c_void_p,
-                                         ctypes.c_int64, _f64p]
+                                         ctypes.c_int64, _f64p, ctypes.c_void_p]
             lib.vo_attention.restype = None
             _lib = lib
     return _lib
@@ -96,8 +96,9 @@ def grid_positions(grid_hw) -> tuple[np.ndarray, np.ndarray]:
 
 
 def norm_rope(x_bits: np.ndarray, pos: np.ndarray, theta: float = 10000.0, w_bits: np.ndarray | None = None,
-              use_norm: bool = False, eps: float = 1e-6) -> np.ndarray:
-    """fp64 RMSNorm (optional) + 2D rotate-half RoPE of bf16 rows x [T, H, D]."""
+              use_norm: bool = False, eps: float = 1e-6, interleaved: bool = False) -> np.ndarray:
+    """fp64 RMSNorm (optional) + 2D RoPE of bf16 rows x [T, H, D]: rotate-half pairs (m, m + D/2), or
+    adjacent pairs (2m, 2m + 1) with ``interleaved`` (the "complex_rope" mode)."""
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     T, H, D = x.shape
     assert D % 4 == 0 and D <= 512
@@ -107,13 +108,15 @@ def norm_rope(x_bits: np.ndarray, pos: np.ndarray, theta: float = 10000.0, w_bit
     w = None if w_bits is None else np.ascontiguousarray(w_bits, dtype=np.uint16).reshape(D)
     _load().vo_norm_rope(x.reshape(-1), T, H, D, H * D, np.ascontiguousarray(pos, dtype=np.int32).reshape(-1),
                          float(theta), None if w is None else w.ctypes.data, int(bool(use_norm)), float(eps),
-                         out.reshape(-1))
+                         int(bool(interleaved)), out.reshape(-1))
     return out
 
 
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_seqlens, scale: float | None = None,
-              rows=None) -> np.ndarray:
-    """Per-segment softmax(scale q k^T) v in fp64; q, k, v fp64 [T, H, D]."""
+              rows=None, return_lse: bool = False):
+    """Per-segment softmax(scale q k^T) v in fp64; q, k, v fp64 [T, H, D].
+
+    With ``return_lse`` also returns lse [n, H] = log sum_j exp(scale <q, k_j>) over each row's segment."""
     q = np.ascontiguousarray(q, dtype=np.float64)
     k = np.ascontiguousarray(k, dtype=np.float64)
     v = np.ascontiguousarray(v, dtype=np.float64)
@@ -128,20 +131,22 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_seqlens, scale: fl
         rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         n = rows_arr.shape[0]
     out = np.zeros((n, H, D), dtype=np.float64)
+    lse = np.zeros((n, H), dtype=np.float64)
     if n == 0 or H == 0:
-        return out
+        return (out, lse) if return_lse else out
     _load().vo_attention(q.reshape(-1), k.reshape(-1), v.reshape(-1), T, H, D, cu, B, float(scale),
-                         None if rows_arr is None else rows_arr.ctypes.data, n, out.reshape(-1))
-    return out
+                         None if rows_arr is None else rows_arr.ctypes.data, n, out.reshape(-1),
+                         lse.ctypes.data if return_lse else None)
+    return (out, lse) if return_lse else out
 
 
 def full_path(grid_hw, q_bits, k_bits, v_bits, norm_w_bits=None, eps: float = 1e-6, theta: float = 10000.0,
-              scale: float | None = None, rows=None) -> np.ndarray:
+              scale: float | None = None, rows=None, interleaved: bool = False, return_lse: bool = False):
     """Positions from the grid, QK-RMSNorm (if weights given) + 2D RoPE, then per-segment attention."""
     cu, pos = grid_positions(grid_hw)
     use_norm = norm_w_bits is not None
     wq = None if norm_w_bits is None else np.asarray(norm_w_bits)[0]
     wk = None if norm_w_bits is None else np.asarray(norm_w_bits)[1]
-    qr = norm_rope(q_bits, pos, theta, wq, use_norm, eps)
-    kr = norm_rope(k_bits, pos, theta, wk, use_norm, eps)
-    return attention(qr, kr, widen(v_bits), cu, scale, rows)
+    qr = norm_rope(q_bits, pos, theta, wq, use_norm, eps, interleaved)
+    kr = norm_rope(k_bits, pos, theta, wk, use_norm, eps, interleaved)
+    return attention(qr, kr, widen(v_bits), cu, scale, rows, return_lse)

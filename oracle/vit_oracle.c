@@ -24,10 +24,19 @@
  *                      MultimodalEncoderAttention.forward, the
  *                      cat([cos, cos]) step); norm before RoPE as in p1
  *                      _VisionAttentionBase._qkv_with_rope.
+ *                      The interleaved mode pairs x[2m] with x[2m+1]
+ *                      instead (p3's "complex_rope" position-embedding mode,
+ *                      MultimodalEncoderAttention.__init__ and the
+ *                      packed_qkv_complex_rotary call in forward: each pair is
+ *                      one complex number turned by the same angle a_m).
  *   vo_attention       per segment of the packed stream and per head:
  *                      softmax(scale * q k^T) v over that segment's keys only
  *                      (p1, VisionAttentionV2.forward: split by segment
- *                      lengths, plain attention per segment, concatenate).
+ *                      lengths, plain attention per segment, concatenate),
+ *                      and optionally the natural-log sum of exp(scale * s)
+ *                      per row (the lse that p3's FA4 and cuDNN backends
+ *                      return next to the output, vision_attn_fa4 and
+ *                      vision_attn_flashinfer_cudnn with return_lse=True).
  *
  * Everything is evaluated in double precision from the exact bf16 inputs
  * (bf16 -> fp64 is exact). No blocking, fusion or reordering beyond the plain
@@ -97,13 +106,16 @@ int64_t vo_grid_positions(const int32_t *grid_hw, int n_img, int32_t *cu, int32_
  * Angles, for pair index m < D/2 (dim = D/2, table of D/4 frequencies):
  *   m <  D/4 : a_m = row * inv_freq[m]
  *   m >= D/4 : a_m = col * inv_freq[m - D/4]
- * Rotate-half with duplicated cos/sin:
+ * Rotate-half with duplicated cos/sin (interleaved == 0):
  *   y[m]       = x[m] cos a_m - x[m + D/2] sin a_m
  *   y[m + D/2] = x[m + D/2] cos a_m + x[m] sin a_m
+ * Interleaved pairs (interleaved != 0):
+ *   y[2m]      = x[2m] cos a_m - x[2m + 1] sin a_m
+ *   y[2m + 1]  = x[2m + 1] cos a_m + x[2m] sin a_m
  */
 void vo_norm_rope(const uint16_t *x, int64_t T, int H, int D, int64_t tok_stride,
                   const int32_t *pos, double theta, const uint16_t *w, int use_norm,
-                  double eps, double *out)
+                  double eps, int interleaved, double *out)
 {
     const int half = D / 2, quarter = D / 4;
     double *inv_freq = (double *)malloc(sizeof(double) * (size_t)(quarter > 0 ? quarter : 1));
@@ -129,8 +141,10 @@ void vo_norm_rope(const uint16_t *x, int64_t T, int H, int D, int64_t tok_stride
             double *o = out + (t * H + h) * (int64_t)D;
             for (int m = 0; m < half; ++m) {
                 double c = cos(ang[m]), s = sin(ang[m]);
-                o[m] = xh[m] * c - xh[m + half] * s;
-                o[m + half] = xh[m + half] * c + xh[m] * s;
+                int i0 = interleaved ? 2 * m : m;           /* the two elements of pair m */
+                int i1 = interleaved ? 2 * m + 1 : m + half;
+                o[i0] = xh[i0] * c - xh[i1] * s;
+                o[i1] = xh[i1] * c + xh[i0] * s;
             }
         }
     }
@@ -141,11 +155,13 @@ void vo_norm_rope(const uint16_t *x, int64_t T, int H, int D, int64_t tok_stride
  * q, k, v: fp64 [T, H, D] contiguous. cu: [B + 1] segment offsets.
  * rows: optional list of n_rows query tokens to evaluate (NULL = all T).
  * out: fp64 [n_rows or T, H, D]; row r of out belongs to rows[r] (or token r).
+ * lse: fp64 [n_rows or T, H] or NULL: log(sum_j exp(scale * <q, k_j>)) over
+ * the row's segment, natural log.
  * A token outside [cu[0], cu[B]) gets NaN (the packing does not cover it).
  */
 void vo_attention(const double *q, const double *k, const double *v, int64_t T, int H, int D,
                   const int32_t *cu, int B, double scale, const int64_t *rows, int64_t n_rows,
-                  double *out)
+                  double *out, double *lse)
 {
     int64_t n = rows ? n_rows : T;
 #pragma omp parallel
@@ -170,6 +186,8 @@ void vo_attention(const double *q, const double *k, const double *v, int64_t T, 
             if (seg < 0) {
                 for (int d = 0; d < D; ++d)
                     o[d] = NAN;
+                if (lse)
+                    lse[r * H + h] = NAN;
                 continue;
             }
             int64_t lo = cu[seg], len = cu[seg + 1] - cu[seg];
@@ -189,6 +207,8 @@ void vo_attention(const double *q, const double *k, const double *v, int64_t T, 
                 s[j] = exp(s[j] - mx);
                 sum += s[j];
             }
+            if (lse)
+                lse[r * H + h] = mx + log(sum);
             for (int d = 0; d < D; ++d)
                 o[d] = 0.0;
             for (int64_t j = 0; j < len; ++j) {

@@ -80,7 +80,7 @@ def test_rope_norm_golden(golden_dir):
         xb = _bits(x).reshape(1, 1, D)
         w = None if case["w"] is None else _bits(case["w"])
         pos = np.array([case["pos"]], dtype=np.int32)
-        y = oracle.norm_rope(xb, pos, 10000.0, w, case["norm"], case["eps"])
+        y = oracle.norm_rope(xb, pos, 10000.0, w, case["norm"], case["eps"], case.get("interleaved", False))
         np.testing.assert_allclose(y.reshape(D), case["y"], rtol=0, atol=1e-14, err_msg=case["what"])
 
 
@@ -101,6 +101,38 @@ def test_rope_matches_complex_rotation():
         np.testing.assert_allclose(y[t, :, D // 2:], z.imag, atol=1e-12)
 
 
+def test_interleaved_rope_matches_complex_rotation():
+    # pair (x[2m], x[2m+1]) as the complex number x[2m] + i x[2m+1] multiplied by exp(i a_m)
+    rng = np.random.default_rng(2)
+    D, H, T = 16, 2, 5
+    xb = wl.bf16_bits(torch.randn(T, H, D).to(torch.bfloat16))
+    x = oracle.widen(xb)
+    pos = rng.integers(0, 300, size=(T, 2)).astype(np.int32)
+    f = 10000.0 ** (-np.arange(D // 4) * 4.0 / D)
+    y = oracle.norm_rope(xb, pos, interleaved=True)
+    for t in range(T):
+        ang = np.concatenate([pos[t, 0] * f, pos[t, 1] * f])
+        z = (x[t, :, 0::2] + 1j * x[t, :, 1::2]) * np.exp(1j * ang)[None]
+        np.testing.assert_allclose(y[t, :, 0::2], z.real, atol=1e-12)
+        np.testing.assert_allclose(y[t, :, 1::2], z.imag, atol=1e-12)
+
+
+def test_interleaved_is_rotate_half_under_a_permutation():
+    # moving element 2m to m and 2m+1 to m + D/2 turns one mode into the other, with norm and weight
+    torch.manual_seed(13)
+    D, H, T = 80, 3, 6
+    x = torch.randn(T, H, D).to(torch.bfloat16)
+    w = (1 + 0.1 * torch.randn(D)).to(torch.bfloat16)
+    perm = np.concatenate([np.arange(0, D, 2), np.arange(1, D, 2)])     # half-layout index -> interleaved index
+    pos = np.random.default_rng(4).integers(0, 64, size=(T, 2)).astype(np.int32)
+    yi = oracle.norm_rope(wl.bf16_bits(x), pos, w_bits=wl.bf16_bits(w), use_norm=True, eps=1e-6, interleaved=True)
+    yh = oracle.norm_rope(wl.bf16_bits(x[..., perm].contiguous()), pos, w_bits=wl.bf16_bits(w[perm].contiguous()),
+                          use_norm=True, eps=1e-6)
+    np.testing.assert_allclose(yi[..., perm], yh, rtol=0, atol=1e-13)
+    assert not np.allclose(yi, oracle.norm_rope(wl.bf16_bits(x), pos, w_bits=wl.bf16_bits(w), use_norm=True,
+                                                eps=1e-6))
+
+
 def test_rope_identity_at_origin_and_pair_norms():
     torch.manual_seed(3)
     D, H, T = 80, 3, 7
@@ -113,6 +145,11 @@ def test_rope_identity_at_origin_and_pair_norms():
     n_in = x[..., : D // 2] ** 2 + x[..., D // 2:] ** 2
     n_out = y[..., : D // 2] ** 2 + y[..., D // 2:] ** 2
     np.testing.assert_allclose(n_out, n_in, rtol=1e-12, atol=1e-12)
+    # the interleaved mode: identity at the origin, adjacent-pair norms kept elsewhere
+    assert np.array_equal(oracle.norm_rope(xb, pos0, interleaved=True), x)
+    yi = oracle.norm_rope(xb, pos, interleaved=True)
+    np.testing.assert_allclose(yi[..., 0::2] ** 2 + yi[..., 1::2] ** 2, x[..., 0::2] ** 2 + x[..., 1::2] ** 2,
+                               rtol=1e-12, atol=1e-12)
 
 
 def test_rope_relative_offsets_only():
@@ -271,3 +308,72 @@ def test_full_path_composes_steps():
     cu, pos = oracle.grid_positions(w.grid_hw)
     ref = dense_block_diag_attention(oracle.norm_rope(qb, pos), oracle.norm_rope(kb, pos), oracle.widen(vb), cu)
     np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- log-sum-exp output
+
+def test_lse_zero_q_is_log_segment_length():
+    # all scores 0: sum of L ones
+    cu = [0, 1, 9, 30, 30, 101]
+    q, k, v = _rand_qkv(101, 3, 8, 91)
+    _, lse = oracle.attention(np.zeros_like(q), k, v, cu, return_lse=True)
+    for s in range(len(cu) - 1):
+        L = cu[s + 1] - cu[s]
+        np.testing.assert_allclose(lse[cu[s]:cu[s + 1]], math.log(L) if L else 0.0, rtol=0, atol=1e-13)
+
+
+def test_lse_geometric_series_closed_form():
+    # q = (c, 0), k_j = (j, 7): scores a*j with a = c*scale, sum_j e^(a j) = (e^(a L) - 1) / (e^a - 1)
+    L, c = 37, 0.3
+    scale = 1.0 / math.sqrt(2)
+    q = np.zeros((L, 1, 2)); q[:, 0, 0] = c
+    k = np.zeros((L, 1, 2)); k[:, 0, 0] = np.arange(L); k[:, 0, 1] = 7.0
+    v = np.ones((L, 1, 2))
+    _, lse = oracle.attention(q, k, v, [0, L], return_lse=True)
+    a = c * scale
+    np.testing.assert_allclose(lse[:, 0], math.log((math.exp(a * L) - 1.0) / (math.exp(a) - 1.0)), rtol=1e-14)
+
+
+def test_lse_single_key_is_the_score():
+    q, k, v = _rand_qkv(4, 2, 16, 92)
+    _, lse = oracle.attention(q, k, v, [0, 1, 2, 3, 4], scale=0.25, return_lse=True)
+    np.testing.assert_allclose(lse, 0.25 * np.sum(q * k, axis=-1), rtol=0, atol=1e-13)
+
+
+def test_lse_equals_library_logsumexp():
+    cu = [0, 5, 5, 17, 18, 40]
+    q, k, v = _rand_qkv(40, 3, 16, 93)
+    out, lse = oracle.attention(q, k, v, cu, scale=0.2, return_lse=True)
+    np.testing.assert_array_equal(out, oracle.attention(q, k, v, cu, scale=0.2))
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        if a == b:
+            continue
+        tq, tk = torch.from_numpy(q[a:b]), torch.from_numpy(k[a:b])
+        sc = torch.einsum("thd,uhd->htu", tq, tk) * 0.2
+        ref = torch.logsumexp(sc, dim=-1).transpose(0, 1).numpy()
+        np.testing.assert_allclose(lse[a:b], ref, rtol=0, atol=1e-12)
+
+
+def test_lse_shifts_with_a_common_key_offset():
+    # adding one vector u to every key of a segment adds scale*<q, u> to every score of its rows:
+    # the lse moves by exactly that, the softmax and the output do not move
+    cu = [0, 11, 30]
+    q, k, v = _rand_qkv(30, 2, 8, 94)
+    out, lse = oracle.attention(q, k, v, cu, return_lse=True)
+    u = np.random.default_rng(5).standard_normal((1, 2, 8))
+    k2 = k.copy(); k2[11:30] += u
+    out2, lse2 = oracle.attention(q, k2, v, cu, return_lse=True)
+    scale = 1.0 / math.sqrt(8)
+    np.testing.assert_allclose(lse2[11:30], lse[11:30] + scale * np.sum(q[11:30] * u, axis=-1), atol=1e-12)
+    assert np.array_equal(lse2[:11], lse[:11])
+    np.testing.assert_allclose(out2, out, atol=1e-12)
+
+
+def test_lse_rows_subset_and_uncovered_token():
+    cu = [0, 13, 40]
+    q, k, v = _rand_qkv(42, 2, 8, 95)
+    _, full = oracle.attention(q, k, v, cu, return_lse=True)
+    _, sub = oracle.attention(q, k, v, cu, rows=[0, 39, 12, 13], return_lse=True)
+    assert np.array_equal(sub, full[[0, 39, 12, 13]])
+    assert np.isnan(full[40:]).all() and np.isfinite(full[:40]).all()
