@@ -132,8 +132,9 @@ class ClockSampler:
 class Path:
     """Device-resident buffers and the three calls of one step."""
 
-    def __init__(self, vit, w: wl.Workload, t: dict, device):
+    def __init__(self, vit, w: wl.Workload, t: dict, device, lse: bool = False, interleaved: bool = False):
         self.vit, self.w = vit, w
+        self.interleaved = interleaved
         T, H, D, B = w.total_tokens, w.heads, w.head_dim, w.num_segments
         self.grid = torch.from_numpy(w.grid_hw.copy()).to(device)
         self.q, self.k, self.v = (t[n].to(device) for n in ("q", "k", "v"))
@@ -141,15 +142,17 @@ class Path:
         self.qr = torch.empty_like(self.q)
         self.kr = torch.empty_like(self.k)
         self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((T, H), dtype=torch.float32, device=device) if lse else None
         self.ws = torch.empty(vit.workspace_size(T, H, B, D), dtype=torch.uint8, device=device)
         self.status = vit.new_status(device)
 
     def step(self):
         vit, w = self.vit, self.w
         inv_freq, pos, cu = vit.rope_freqs(self.grid, w.total_tokens, w.head_dim, w.theta, status=self.status)
-        vit.qk_norm_rope(self.q, self.k, pos, inv_freq, self.nw, w.eps, q_out=self.qr, k_out=self.kr)
+        vit.qk_norm_rope(self.q, self.k, pos, inv_freq, self.nw, w.eps, q_out=self.qr, k_out=self.kr,
+                         interleaved=self.interleaved)
         vit.varlen_attn(self.qr, self.kr, self.v, cu, w.max_seqlen, out=self.out, workspace=self.ws,
-                        status=self.status)
+                        status=self.status, lse=self.lse)
 
 
 def e2e_step(vit, w, host, device, stream):
@@ -234,7 +237,7 @@ def run_ours(args, rank, world, local):
     w = wl.make_config(args.config)
     t = w.tensors()
     T, H, D = w.total_tokens, w.heads, w.head_dim
-    path = Path(vit, w, t, device)
+    path = Path(vit, w, t, device, lse=args.lse, interleaved=args.interleaved)
     stream = torch.cuda.current_stream()
     tensor_bytes = T * H * D * 2
     working_set = 6 * tensor_bytes
@@ -348,6 +351,7 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "tokens": T, "segments": w.num_segments, "heads": H, "head_dim": D,
                    "qk_norm": w.qk_norm, "max_seqlen": w.max_seqlen, "useful_flops_per_step": flops,
+                   "rope": "interleaved" if args.interleaved else "rotate_half", "lse": bool(args.lse),
                    "l2": "L2 flushed between steps" if flush else
                    f"inputs larger than L2 ({working_set / 2 ** 20:.0f} MiB working set)",
                    "parallelism": "replicas" if world > 1 else "single"},
@@ -456,6 +460,9 @@ def main():
     ap.add_argument("--short-max", type=int, default=None,
                     help="segments longer than this run on the tcgen05 kernel (library default 64)")
     ap.add_argument("--ref-rows", type=int, default=16)
+    ap.add_argument("--lse", action="store_true", help="also write the per-row log-sum-exp [T, H] each step")
+    ap.add_argument("--interleaved", action="store_true",
+                    help="rotate adjacent pairs (the complex_rope mode) instead of (m, m + D/2)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

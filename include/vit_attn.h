@@ -134,6 +134,39 @@ vit_status_t vit_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, v
                               const int32_t *pos_hw, const float *inv_freq,
                               const void *norm_w, float eps, vit_stream_t stream);
 
+/* Rotary pairings of vit_qk_norm_rope_ex. */
+enum {
+    VIT_ROPE_ROTATE_HALF = 0,   /* pairs (m, m + D/2): the NeoX layout of vit_qk_norm_rope */
+    VIT_ROPE_INTERLEAVED = 1    /* pairs (2m, 2m + 1) */
+};
+
+/*
+ * vit_qk_norm_rope with a choice of rotary pairing.
+ *
+ * [TS] MultimodalEncoderAttention accepts position_embedding_mode
+ * "complex_rope" and then rotates q and k with packed_qkv_complex_rotary; the
+ * page does not print that routine. It is read here as the complex form of
+ * the same rotation: element pair m is (x[2m], x[2m + 1]), one complex number
+ * turned by the same angle a_m as in the rotate-half mode:
+ *   y[2m]     = x[2m] cos a_m - x[2m + 1] sin a_m
+ *   y[2m + 1] = x[2m + 1] cos a_m + x[2m] sin a_m
+ * RMSNorm (if norm_w is given) is the same in both modes.
+ *
+ * Arguments as for vit_qk_norm_rope, plus:
+ *   rope_mode   VIT_ROPE_ROTATE_HALF or VIT_ROPE_INTERLEAVED (else
+ *               VIT_ERR_BAD_ARGUMENT).
+ * In both calls either half may be left out: q_in and q_out both NULL skip q
+ * (its strides are then ignored), k_in and k_out both NULL skip k. Passing
+ * only one pointer of a pair, or leaving out both halves, is
+ * VIT_ERR_NULL_POINTER.
+ */
+vit_status_t vit_qk_norm_rope_ex(const void *q_in, void *q_out, const void *k_in, void *k_out,
+                                 int64_t T, int H, int D,
+                                 int64_t q_in_stride, int64_t q_out_stride,
+                                 int64_t k_in_stride, int64_t k_out_stride,
+                                 const int32_t *pos_hw, const float *inv_freq,
+                                 const void *norm_w, float eps, int rope_mode, vit_stream_t stream);
+
 /*
  * Workspace bytes vit_varlen_attn needs for these sizes (an upper bound
  * independent of the segment lengths). Returns 0 for invalid sizes.
@@ -170,6 +203,27 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
                              const int32_t *cu_seqlens, int B, int max_seqlen, float scale,
                              void *out, int64_t out_stride, void *workspace, size_t workspace_bytes,
                              int32_t *status_dev, vit_stream_t stream);
+
+/*
+ * vit_varlen_attn that also returns each row's log-sum-exp.
+ *
+ * [TS] vision_attn_fa4 notes that the FA4 kernel returns (output, lse) and
+ * vision_attn_flashinfer_cudnn calls cuDNN with return_lse=True; the value is
+ * what lets a caller merge partial attentions or recompute the softmax. Here:
+ *   lse[t, h] = ln( sum_j exp(scale * <q[t, h], k[j, h]>) ), j in t's segment,
+ * computed from the kernels' fp32 running max and row sum.
+ *
+ * Arguments as for vit_varlen_attn, plus:
+ *   lse   device fp32 [T, H] (token-major, contiguous, 4-byte aligned), or
+ *         NULL (then identical to vit_varlen_attn). Rows of zero-length
+ *         segments do not exist; every other row is written.
+ */
+vit_status_t vit_varlen_attn_lse(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                 int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                                 const int32_t *cu_seqlens, int B, int max_seqlen, float scale,
+                                 void *out, int64_t out_stride, float *lse,
+                                 void *workspace, size_t workspace_bytes,
+                                 int32_t *status_dev, vit_stream_t stream);
 
 /* Size of the fixed device scratch array behind vit_varlen_attn_noalloc (per GPU). */
 #define VIT_NOALLOC_WORKSPACE_BYTES (4u << 20)

@@ -105,6 +105,29 @@ def test_prologue_and_rope_validation_without_gpu(L):
     assert L.vit_rope_freqs(40, 10000.0, p(16), 1, 4, None, None, None, None, None) == 0
 
 
+def test_extended_calls_validation_without_gpu(L):
+    p = ctypes.c_void_p
+    ex = L.vit_qk_norm_rope_ex
+    good = dict(qi=16, qo=16, ki=16, ko=16, mode=0)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return ex(p(a["qi"]) if a["qi"] else None, p(a["qo"]) if a["qo"] else None,
+                  p(a["ki"]) if a["ki"] else None, p(a["ko"]) if a["ko"] else None, 10, 2, 80, 160, 160, 160, 160,
+                  p(16), p(16), None, 1e-6, a["mode"], None)
+    assert call(mode=2) == -14                       # unknown rotary pairing
+    assert call(mode=-1) == -14
+    assert call(qo=0) == -1                          # half a q pair
+    assert call(ki=0) == -1                          # half a k pair
+    assert call(qi=0, qo=0, ki=0, ko=0) == -1        # nothing to do is a caller error
+    # vit_varlen_attn_lse: same checks as vit_varlen_attn plus the lse alignment
+    args = [p(16), p(16), p(16), 128, 2, 80, 160, 160, 160, p(16), 1, 128, 0.0, p(16), 160]
+    assert L.vit_varlen_attn_lse(*args, p(18), p(256), 1 << 20, None, None) == -5
+    args_bad = list(args)
+    args_bad[5] = 81
+    assert L.vit_varlen_attn_lse(*args_bad, p(16), p(256), 1 << 20, None, None) == -2
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import importlib
     monkeypatch.setattr(vit, "_lib", None)

@@ -53,10 +53,14 @@ def lib() -> ctypes.CDLL:
             L.vit_device_supported.argtypes = [i32]
             L.vit_rope_freqs.argtypes = [i32, f32, vp, i32, i64, vp, vp, vp, vp, vp]
             L.vit_qk_norm_rope.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i64, i64, vp, vp, vp, f32, vp]
+            L.vit_qk_norm_rope_ex.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i64, i64, vp, vp, vp, f32,
+                                              i32, vp]
             L.vit_varlen_attn_workspace_size.restype = sz
             L.vit_varlen_attn_workspace_size.argtypes = [i64, i32, i32, i32]
             L.vit_varlen_attn.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, vp, i32, i32, f32, vp, i64, vp,
                                           sz, vp, vp]
+            L.vit_varlen_attn_lse.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, vp, i32, i32, f32, vp, i64,
+                                              vp, vp, sz, vp, vp]
             L.vit_read_status.argtypes = [vp, vp]
             L.vit_set_short_segment_max.argtypes = [i32]
             L.vit_set_short_segment_max.restype = i32
@@ -65,8 +69,9 @@ def lib() -> ctypes.CDLL:
             L.vit_launch_count.restype = i64
             L.vit_kernel_timing.argtypes = [i32]
             L.vit_kernel_timing_read.argtypes = [ctypes.POINTER(_KernelTime), i32]
-            for fn in ("vit_device_supported", "vit_rope_freqs", "vit_qk_norm_rope", "vit_varlen_attn",
-                       "vit_read_status", "vit_kernel_timing", "vit_kernel_timing_read"):
+            for fn in ("vit_device_supported", "vit_rope_freqs", "vit_qk_norm_rope", "vit_qk_norm_rope_ex",
+                       "vit_varlen_attn", "vit_varlen_attn_lse", "vit_read_status", "vit_kernel_timing",
+                       "vit_kernel_timing_read"):
                 getattr(L, fn).restype = i32
             _lib = L
     return _lib
@@ -131,27 +136,42 @@ def rope_freqs(grid_hw: torch.Tensor, total_tokens: int, head_dim: int, theta: f
     return inv_freq, pos, cu
 
 
-def qk_norm_rope(q: torch.Tensor, k: torch.Tensor, pos_hw: torch.Tensor, inv_freq: torch.Tensor,
+ROPE_ROTATE_HALF = 0    # pairs (m, m + D/2)
+ROPE_INTERLEAVED = 1    # pairs (2m, 2m + 1), the "complex_rope" mode
+
+
+def qk_norm_rope(q: torch.Tensor | None, k: torch.Tensor | None, pos_hw: torch.Tensor, inv_freq: torch.Tensor,
                  norm_w: torch.Tensor | None = None, eps: float = 1e-6, *, q_out: torch.Tensor | None = None,
-                 k_out: torch.Tensor | None = None, inplace: bool = False, stream=None):
-    """QK-RMSNorm (if norm_w [2, D] is given) + 2D RoPE. Returns (q', k')."""
-    T, H, D = q.shape
-    qs = _tok_stride(q, "q", H, D)
-    ks = _tok_stride(k, "k", H, D)
+                 k_out: torch.Tensor | None = None, inplace: bool = False, interleaved: bool = False, stream=None):
+    """QK-RMSNorm (if norm_w [2, D] is given) + 2D RoPE. Returns (q', k'); a half passed as None is
+    skipped and returned as None. ``interleaved`` rotates adjacent pairs instead of (m, m + D/2)."""
+    ref = q if q is not None else k
+    if ref is None:
+        raise ValueError("at least one of q and k is required")
+    T, H, D = ref.shape
+    qs = _tok_stride(q, "q", H, D) if q is not None else 0
+    ks = _tok_stride(k, "k", H, D) if k is not None else 0
+    if q is not None and k is not None and q.shape[0] != k.shape[0]:
+        raise ValueError("q and k must have the same number of tokens")
     if inplace:
         q_out, k_out = q, k
-    if q_out is None:
+    if q is not None and q_out is None:
         q_out = torch.empty((T, H, D), dtype=q.dtype, device=q.device)
-    if k_out is None:
+    if k is not None and k_out is None:
         k_out = torch.empty((T, H, D), dtype=k.dtype, device=k.device)
-    qos = _tok_stride(q_out, "q_out", H, D)
-    kos = _tok_stride(k_out, "k_out", H, D)
+    if q is None:
+        q_out = None
+    if k is None:
+        k_out = None
+    qos = _tok_stride(q_out, "q_out", H, D) if q_out is not None else 0
+    kos = _tok_stride(k_out, "k_out", H, D) if k_out is not None else 0
     if norm_w is not None and (norm_w.dtype != torch.bfloat16 or norm_w.numel() != 2 * D
                                or not norm_w.is_contiguous()):
         raise ValueError("norm_w must be a contiguous bfloat16 tensor [2, D]")
-    _check(lib().vit_qk_norm_rope(_ptr(q), _ptr(q_out), _ptr(k), _ptr(k_out), T, H, D, qs, qos, ks, kos,
-                                  _ptr(pos_hw), _ptr(inv_freq), _ptr(norm_w), float(eps), _stream(stream)),
-           "vit_qk_norm_rope")
+    mode = ROPE_INTERLEAVED if interleaved else ROPE_ROTATE_HALF
+    _check(lib().vit_qk_norm_rope_ex(_ptr(q), _ptr(q_out), _ptr(k), _ptr(k_out), T, H, D, qs, qos, ks, kos,
+                                     _ptr(pos_hw), _ptr(inv_freq), _ptr(norm_w), float(eps), mode, _stream(stream)),
+           "vit_qk_norm_rope_ex")
     return q_out, k_out
 
 
@@ -162,8 +182,12 @@ def workspace_size(T: int, H: int, B: int, D: int) -> int:
 def varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor | None,
                 max_seqlen: int, scale: float | None = None, *, num_segments: int | None = None,
                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Non-causal attention inside each packed segment. q, k, v [T, H, D] bf16 -> out [T, H, D] bf16."""
+                status: torch.Tensor | None = None, return_lse: bool = False, lse: torch.Tensor | None = None,
+                stream=None):
+    """Non-causal attention inside each packed segment. q, k, v [T, H, D] bf16 -> out [T, H, D] bf16.
+
+    With ``return_lse`` (or an ``lse`` buffer) also returns lse [T, H] fp32, the natural-log
+    sum of exp(scale * q.k) over each row's segment: (out, lse)."""
     T, H, D = q.shape
     qs, ks, vs = _tok_stride(q, "q", H, D), _tok_stride(k, "k", H, D), _tok_stride(v, "v", H, D)
     if cu_seqlens is not None:
@@ -180,11 +204,21 @@ def varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: t
     need = workspace_size(T, H, B, D)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    _check(lib().vit_varlen_attn(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, _ptr(cu_seqlens), B,
-                                 int(max_seqlen), float(scale) if scale is not None else 0.0, _ptr(out), os_,
-                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
-                                 _stream(stream)), "vit_varlen_attn")
-    return out
+    sc = float(scale) if scale is not None else 0.0
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if not return_lse and lse is None:
+        _check(lib().vit_varlen_attn(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, _ptr(cu_seqlens), B,
+                                     int(max_seqlen), sc, _ptr(out), os_, _ptr(workspace), ws_bytes, _ptr(status),
+                                     _stream(stream)), "vit_varlen_attn")
+        return out
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (T, H) or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError(f"lse must be a contiguous CUDA float32 tensor [{T}, {H}]")
+    _check(lib().vit_varlen_attn_lse(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, _ptr(cu_seqlens), B,
+                                     int(max_seqlen), sc, _ptr(out), os_, _ptr(lse), _ptr(workspace), ws_bytes,
+                                     _ptr(status), _stream(stream)), "vit_varlen_attn_lse")
+    return out, lse
 
 
 def set_short_segment_max(short_max: int) -> int:

@@ -113,29 +113,45 @@ vit_status_t vit_rope_freqs(int dim, float theta, const int32_t *grid_hw, int n_
                                        (cudaStream_t)stream));
 }
 
-vit_status_t vit_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T, int H, int D,
-                              int64_t q_in_stride, int64_t q_out_stride, int64_t k_in_stride, int64_t k_out_stride,
-                              const int32_t *pos_hw, const float *inv_freq, const void *norm_w, float eps,
-                              vit_stream_t stream)
+vit_status_t vit_qk_norm_rope_ex(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T, int H,
+                                 int D, int64_t q_in_stride, int64_t q_out_stride, int64_t k_in_stride,
+                                 int64_t k_out_stride, const int32_t *pos_hw, const float *inv_freq,
+                                 const void *norm_w, float eps, int rope_mode, vit_stream_t stream)
 {
     if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
     if (T < 0 || T >= kMaxTokens || H < 1) return VIT_ERR_BAD_SHAPE;
     if (!(eps >= 0.f) || !isfinite(eps)) return VIT_ERR_BAD_ARGUMENT;
+    if (rope_mode != VIT_ROPE_ROTATE_HALF && rope_mode != VIT_ROPE_INTERLEAVED) return VIT_ERR_BAD_ARGUMENT;
+    // each of the q and k halves is either fully given or fully absent; at least one is given
+    const bool has_q = q_in || q_out, has_k = k_in || k_out;
+    if ((has_q && (!q_in || !q_out)) || (has_k && (!k_in || !k_out)) || (!has_q && !has_k))
+        return VIT_ERR_NULL_POINTER;
     if (T == 0) return VIT_OK;
-    if (!q_in || !q_out || !k_in || !k_out || !pos_hw || !inv_freq) return VIT_ERR_NULL_POINTER;
-    if (!stride_ok(q_in_stride, H, D) || !stride_ok(q_out_stride, H, D) || !stride_ok(k_in_stride, H, D) ||
-        !stride_ok(k_out_stride, H, D))
+    if (!pos_hw || !inv_freq) return VIT_ERR_NULL_POINTER;
+    if ((has_q && (!stride_ok(q_in_stride, H, D) || !stride_ok(q_out_stride, H, D))) ||
+        (has_k && (!stride_ok(k_in_stride, H, D) || !stride_ok(k_out_stride, H, D))))
         return VIT_ERR_BAD_STRIDE;
-    if ((q_in == q_out && q_in_stride != q_out_stride) || (k_in == k_out && k_in_stride != k_out_stride))
+    if ((has_q && q_in == q_out && q_in_stride != q_out_stride) ||
+        (has_k && k_in == k_out && k_in_stride != k_out_stride))
         return VIT_ERR_BAD_STRIDE;
-    if (!aligned16(q_in) || !aligned16(q_out) || !aligned16(k_in) || !aligned16(k_out) ||
+    if ((has_q && (!aligned16(q_in) || !aligned16(q_out))) || (has_k && (!aligned16(k_in) || !aligned16(k_out))) ||
         ((uintptr_t)pos_hw & 7u) || ((uintptr_t)inv_freq & 3u) || ((uintptr_t)norm_w & 1u))
         return VIT_ERR_MISALIGNED;
     int sms = 0;
     vit_status_t st = device_info(&sms);
     if (st != VIT_OK) return st;
     return from_cuda(launch_qk_norm_rope(q_in, q_out, k_in, k_out, T, H, D, q_in_stride, q_out_stride, k_in_stride,
-                                         k_out_stride, pos_hw, inv_freq, norm_w, eps, sms, (cudaStream_t)stream));
+                                         k_out_stride, pos_hw, inv_freq, norm_w, eps,
+                                         rope_mode == VIT_ROPE_INTERLEAVED, sms, (cudaStream_t)stream));
+}
+
+vit_status_t vit_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T, int H, int D,
+                              int64_t q_in_stride, int64_t q_out_stride, int64_t k_in_stride, int64_t k_out_stride,
+                              const int32_t *pos_hw, const float *inv_freq, const void *norm_w, float eps,
+                              vit_stream_t stream)
+{
+    return vit_qk_norm_rope_ex(q_in, q_out, k_in, k_out, T, H, D, q_in_stride, q_out_stride, k_in_stride,
+                               k_out_stride, pos_hw, inv_freq, norm_w, eps, VIT_ROPE_ROTATE_HALF, stream);
 }
 
 size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D)
@@ -147,10 +163,10 @@ size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D)
     return sizeof(WsHeader) + sizeof(Item) * (size_t)items;
 }
 
-vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_t T, int H, int D, int64_t q_stride,
-                             int64_t k_stride, int64_t v_stride, const int32_t *cu_seqlens, int B, int max_seqlen,
-                             float scale, void *out, int64_t out_stride, void *workspace, size_t workspace_bytes,
-                             int32_t *status_dev, vit_stream_t stream)
+vit_status_t vit_varlen_attn_lse(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                 int64_t q_stride, int64_t k_stride, int64_t v_stride, const int32_t *cu_seqlens,
+                                 int B, int max_seqlen, float scale, void *out, int64_t out_stride, float *lse,
+                                 void *workspace, size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
 {
     if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
     if (T < 0 || T >= kMaxTokens || H < 1 || B < 0) return VIT_ERR_BAD_SHAPE;
@@ -165,6 +181,7 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
             !stride_ok(out_stride, H, D))
             return VIT_ERR_BAD_STRIDE;
         if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return VIT_ERR_MISALIGNED;
+        if ((uintptr_t)lse & 3u) return VIT_ERR_MISALIGNED;
     }
     if (!workspace) return VIT_ERR_NULL_POINTER;
     if (!aligned16(workspace) || ((uintptr_t)cu_seqlens & 3u)) return VIT_ERR_MISALIGNED;
@@ -176,7 +193,6 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
     vit_status_t st = device_info(&sms);
     if (st != VIT_OK) return st;
     if (scale <= 0.f) scale = 1.0f / sqrtf((float)D);
-    const float scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t s = (cudaStream_t)stream;
 
     WsHeader *hdr = static_cast<WsHeader *>(workspace);
@@ -188,18 +204,40 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
     cudaError_t e = launch_schedule(cu_seqlens, B, T, H, max_seqlen, sp, hdr, items, status_dev, s);
     if (e != cudaSuccess) return VIT_ERR_CUDA;
     if (T == 0) return VIT_OK;
+    AttnArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.lse = lse;
+    a.T = T;
+    a.H = H;
+    a.D = D;
+    a.q_stride = q_stride;
+    a.k_stride = k_stride;
+    a.v_stride = v_stride;
+    a.out_stride = out_stride;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.hdr = hdr;
+    a.items = items;
+    a.status = status_dev;
     // a segment can only be long when the bound allows it
     const int64_t longest = cu_seqlens ? (int64_t)max_seqlen : T / B;
     if (longest > sp.short_max) {
-        e = launch_attn_long(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, D, scale_log2, hdr, items,
-                             max_items(T, H, B, sp.bm_long), sms, status_dev, g_stall_v.load(), s);
+        e = launch_attn_long(a, max_items(T, H, B, sp.bm_long), sms, g_stall_v.load(), s);
         if (e != cudaSuccess) return VIT_ERR_CUDA;
     }
-    if (sp.short_max > 0) {
-        e = launch_attn_short(q, k, v, q_stride, k_stride, v_stride, out, out_stride, D, scale_log2, hdr, items,
-                              max_items(T, H, B, sp.bm_short), sms, s);
-    }
+    if (sp.short_max > 0) e = launch_attn_short(a, max_items(T, H, B, sp.bm_short), sms, s);
     return from_cuda(e);
+}
+
+vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_t T, int H, int D, int64_t q_stride,
+                             int64_t k_stride, int64_t v_stride, const int32_t *cu_seqlens, int B, int max_seqlen,
+                             float scale, void *out, int64_t out_stride, void *workspace, size_t workspace_bytes,
+                             int32_t *status_dev, vit_stream_t stream)
+{
+    return vit_varlen_attn_lse(q, k, v, T, H, D, q_stride, k_stride, v_stride, cu_seqlens, B, max_seqlen, scale, out,
+                               out_stride, nullptr, workspace, workspace_bytes, status_dev, stream);
 }
 
 int vit_debug_stall_long_kernel(int enable)

@@ -88,12 +88,12 @@ struct Bars {
 
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_addr(&b); }
 
-template <int D>
+template <int D, bool LSE>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out, int64_t out_stride,
-                 float scale_log2, const WsHeader *__restrict__ hdr, const Item *__restrict__ items,
-                 int32_t *status, int stall_v)
+                 float *__restrict__ lse, int H, float scale_log2, const WsHeader *__restrict__ hdr,
+                 const Item *__restrict__ items, int32_t *status, int stall_v)
 {
     using C = LongCfg<D>;
     constexpr int BN = C::BN, ST = C::STAGES, NSLAB = C::NSLAB;
@@ -404,6 +404,8 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int q_row = q0 + grp * BM + row;
             const bool store = q_row < seg0 + seg_len;
             const float inv_l = 1.f / l_run;
+            // l_run sums exp2(s * scale*log2(e) - m_run), so ln(sum exp(scale * s)) = (m_run + log2 l_run) ln 2
+            if (LSE && store) lse[(int64_t)q_row * H + head] = (m_run + log2f(l_run)) * 0.6931471805599453f;
             __nv_bfloat16 *dst = out + (int64_t)q_row * out_stride + (int64_t)head * D;
 #pragma unroll
             for (int c = 0; c < D; c += 16) {
@@ -466,27 +468,28 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int D, int64_t 
 }
 
 template <int D>
-cudaError_t launch_d(const void *q, const void *k, const void *v, int64_t T, int H, int64_t qs, int64_t ks,
-                     int64_t vs, void *out, int64_t os, float scale_log2, const WsHeader *hdr, const Item *items,
-                     int64_t max_items, int num_sms, int32_t *status, int stall_v, cudaStream_t stream)
+cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, int stall_v, cudaStream_t stream)
 {
     using C = LongCfg<D>;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, T, H, D, qs, BM) || !make_map(&mk, k, T, H, D, ks, C::BN) ||
-        !make_map(&mv, v, T, H, D, vs, C::BN))
+    if (!make_map(&mq, a.q, a.T, a.H, D, a.q_stride, BM) || !make_map(&mk, a.k, a.T, a.H, D, a.k_stride, C::BN) ||
+        !make_map(&mv, a.v, a.T, a.H, D, a.v_stride, C::BN))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(attn_long_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    // the lse store is compiled in only where it is asked for: the plain kernel keeps its code unchanged
+    auto kern = a.lse ? attn_long_kernel<D, true> : attn_long_kernel<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     // the setmaxnreg split assumes exactly this launch budget; refuse anything else rather than wait on it
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_long_kernel<D>);
+    e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
     const unsigned blocks = (unsigned)(max_items < num_sms ? max_items : num_sms);
     if (blocks == 0) return cudaSuccess;
     LaunchScope scope("attn_long", stream);
-    attn_long_kernel<D><<<blocks, kThreads, C::SMEM, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16 *>(out), os,
-                                                               scale_log2, hdr, items, status, stall_v);
+    kern<<<blocks, kThreads, C::SMEM, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16 *>(a.out),
+                                                               a.out_stride, a.lse, a.H, a.scale_log2, a.hdr,
+                                                               a.items, a.status, stall_v);
     return cudaGetLastError();
 }
 
@@ -496,17 +499,15 @@ int attn_long_bm() { return 2 * BM; }
 
 bool attn_long_supports(int D) { return D == 32 || D == 64 || D == 80 || D == 96 || D == 128; }
 
-cudaError_t launch_attn_long(const void *q, const void *k, const void *v, int64_t T, int H, int64_t q_stride,
-                             int64_t k_stride, int64_t v_stride, void *out, int64_t out_stride, int D,
-                             float scale_log2, const WsHeader *hdr, const Item *items, int64_t max_items_long,
-                             int num_sms, int32_t *status, int stall_v, cudaStream_t stream)
+cudaError_t launch_attn_long(const AttnArgs &a, int64_t max_items_long, int num_sms, int stall_v,
+                             cudaStream_t stream)
 {
-    switch (D) {
-        case 32: return launch_d<32>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stall_v, stream);
-        case 64: return launch_d<64>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stall_v, stream);
-        case 80: return launch_d<80>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stall_v, stream);
-        case 96: return launch_d<96>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stall_v, stream);
-        case 128: return launch_d<128>(q, k, v, T, H, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_long, num_sms, status, stall_v, stream);
+    switch (a.D) {
+        case 32: return launch_d<32>(a, max_items_long, num_sms, stall_v, stream);
+        case 64: return launch_d<64>(a, max_items_long, num_sms, stall_v, stream);
+        case 80: return launch_d<80>(a, max_items_long, num_sms, stall_v, stream);
+        case 96: return launch_d<96>(a, max_items_long, num_sms, stall_v, stream);
+        case 128: return launch_d<128>(a, max_items_long, num_sms, stall_v, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -98,8 +98,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, ShortCfg<D>::MIN_BLOCKS)
 attn_short_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                   const __nv_bfloat16 *__restrict__ v, int64_t q_stride, int64_t k_stride, int64_t v_stride,
-                  __nv_bfloat16 *__restrict__ out, int64_t out_stride, float scale_log2,
-                  const WsHeader *__restrict__ hdr, const Item *__restrict__ items)
+                  __nv_bfloat16 *__restrict__ out, int64_t out_stride, float *__restrict__ lse, int H,
+                  float scale_log2, const WsHeader *__restrict__ hdr, const Item *__restrict__ items)
 {
     using C = ShortCfg<D>;
     constexpr int PITCH = C::PITCH;
@@ -268,6 +268,12 @@ attn_short_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
                 }
                 const float inv0 = 1.f / l_r[mt][0], inv1 = 1.f / l_r[mt][1];
                 const int r0 = r_base + mt * 16 + g, r1 = r0 + 8;
+                if (lse && tig == 0) {                       // ln(sum exp(scale * s)) = (m + log2 l) ln 2
+                    if (r0 < q_valid)
+                        lse[(int64_t)(q0 + r0) * H + head] = (m_r[mt][0] + log2f(l_r[mt][0])) * 0.6931471805599453f;
+                    if (r1 < q_valid)
+                        lse[(int64_t)(q0 + r1) * H + head] = (m_r[mt][1] + log2f(l_r[mt][1])) * 0.6931471805599453f;
+                }
 #pragma unroll
                 for (int nd = 0; nd < DN; ++nd) {
                     const int col = nd * 8 + tig * 2;
@@ -284,9 +290,7 @@ attn_short_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
 }
 
 template <int D>
-cudaError_t launch_d(const void *q, const void *k, const void *v, int64_t qs, int64_t ks, int64_t vs, void *out,
-                     int64_t os, float scale_log2, const WsHeader *hdr, const Item *items, int64_t max_items,
-                     int num_sms, cudaStream_t stream)
+cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, cudaStream_t stream)
 {
     constexpr size_t smem = ShortCfg<D>::SMEM;
     static_assert(smem <= 227 * 1024, "shared memory budget");
@@ -300,9 +304,9 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, int64_t qs, in
     if (blocks == 0) return cudaSuccess;
     LaunchScope scope("attn_short", stream);
     attn_short_kernel<D><<<blocks, kThreads, smem, stream>>>(
-        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-        static_cast<const __nv_bfloat16 *>(v), qs, ks, vs, static_cast<__nv_bfloat16 *>(out), os, scale_log2, hdr,
-        items);
+        static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k),
+        static_cast<const __nv_bfloat16 *>(a.v), a.q_stride, a.k_stride, a.v_stride,
+        static_cast<__nv_bfloat16 *>(a.out), a.out_stride, a.lse, a.H, a.scale_log2, a.hdr, a.items);
     return cudaGetLastError();
 }
 
@@ -310,17 +314,14 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, int64_t qs, in
 
 int attn_short_bm() { return BM; }
 
-cudaError_t launch_attn_short(const void *q, const void *k, const void *v, int64_t q_stride, int64_t k_stride,
-                              int64_t v_stride, void *out, int64_t out_stride, int D, float scale_log2,
-                              const WsHeader *hdr, const Item *items, int64_t max_items_short, int num_sms,
-                              cudaStream_t stream)
+cudaError_t launch_attn_short(const AttnArgs &a, int64_t max_items_short, int num_sms, cudaStream_t stream)
 {
-    switch (D) {
-        case 32: return launch_d<32>(q, k, v, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_short, num_sms, stream);
-        case 64: return launch_d<64>(q, k, v, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_short, num_sms, stream);
-        case 80: return launch_d<80>(q, k, v, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_short, num_sms, stream);
-        case 96: return launch_d<96>(q, k, v, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_short, num_sms, stream);
-        case 128: return launch_d<128>(q, k, v, q_stride, k_stride, v_stride, out, out_stride, scale_log2, hdr, items, max_items_short, num_sms, stream);
+    switch (a.D) {
+        case 32: return launch_d<32>(a, max_items_short, num_sms, stream);
+        case 64: return launch_d<64>(a, max_items_short, num_sms, stream);
+        case 80: return launch_d<80>(a, max_items_short, num_sms, stream);
+        case 96: return launch_d<96>(a, max_items_short, num_sms, stream);
+        case 128: return launch_d<128>(a, max_items_short, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

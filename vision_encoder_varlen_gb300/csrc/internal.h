@@ -56,24 +56,34 @@ cudaError_t launch_rope_freqs(int dim, float theta, const int32_t *grid_hw, int 
                               float *inv_freq, int32_t *pos_hw, int32_t *cu_seqlens, int32_t *status,
                               cudaStream_t stream);
 
+// q_in/q_out or k_in/k_out may both be NULL (that half is skipped); interleaved selects adjacent pairs.
 cudaError_t launch_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T,
                                 int H, int D, int64_t q_in_stride, int64_t q_out_stride,
                                 int64_t k_in_stride, int64_t k_out_stride, const int32_t *pos_hw,
-                                const float *inv_freq, const void *norm_w, float eps, int num_sms,
-                                cudaStream_t stream);
+                                const float *inv_freq, const void *norm_w, float eps, bool interleaved,
+                                int num_sms, cudaStream_t stream);
 
 cudaError_t launch_schedule(const int32_t *cu_seqlens, int B, int64_t T, int H, int max_seqlen,
                             SchedParams sp, WsHeader *hdr, Item *items, int32_t *status,
                             cudaStream_t stream);
 
-cudaError_t launch_attn_short(const void *q, const void *k, const void *v, int64_t q_stride,
-                              int64_t k_stride, int64_t v_stride, void *out, int64_t out_stride,
-                              int D, float scale_log2, const WsHeader *hdr, const Item *items,
-                              int64_t max_items_short, int num_sms, cudaStream_t stream);
+// Everything both attention kernels read, validated by the API layer.
+struct AttnArgs {
+    const void *q, *k, *v;      // bf16 [T, H, D] with token strides below
+    void *out;                  // bf16 [T, H, D]
+    float *lse;                 // fp32 [T, H] natural-log sum of exp(scale * s) per row, or NULL
+    int64_t T;
+    int H, D;
+    int64_t q_stride, k_stride, v_stride, out_stride;   // token strides, elements
+    float scale_log2;           // softmax scale * log2(e)
+    const WsHeader *hdr;
+    const Item *items;
+    int32_t *status;
+};
 
-cudaError_t launch_attn_long(const void *q, const void *k, const void *v, int64_t T, int H, int64_t q_stride,
-                             int64_t k_stride, int64_t v_stride, void *out, int64_t out_stride, int D,
-                             float scale_log2, const WsHeader *hdr, const Item *items, int64_t max_items_long,
-                             int num_sms, int32_t *status, int stall_v, cudaStream_t stream);
+cudaError_t launch_attn_short(const AttnArgs &a, int64_t max_items_short, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_attn_long(const AttnArgs &a, int64_t max_items_long, int num_sms, int stall_v,
+                             cudaStream_t stream);
 
 }  // namespace vit

@@ -16,6 +16,12 @@
 // three-step shuffle inside the group. Each group issues the loads of four rows
 // before it computes on any of them, to keep enough bytes in flight.
 // HBM-bound: 8*T*H*D bytes move in total.
+//
+// The interleaved mode (tokenspeed mm_encoder_attention.py, the "complex_rope"
+// position-embedding mode and packed_qkv_complex_rotary) pairs x[2m] with
+// x[2m+1] and turns the pair by the same angle a_m; a lane then rotates pairs
+// inside each of its two chunks. Either q or k may be left out (its pointers
+// NULL), which turns the pass into a one-tensor pre-stage.
 #include "internal.h"
 
 namespace vit {
@@ -76,7 +82,7 @@ __device__ __forceinline__ void norm_pair(float &x0, float &x1, float inv, uint3
     x1 = __uint_as_float(u & 0xffff0000u);
 }
 
-template <int D>
+template <int D, bool IL>
 __global__ void __launch_bounds__(kThreads)
 qk_norm_rope_kernel(const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out,
                     const __nv_bfloat16 *k_in, __nv_bfloat16 *k_out, int64_t T, int H,
@@ -97,7 +103,8 @@ qk_norm_rope_kernel(const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out,
         for (int i = tid; i < D; i += kThreads)
             s_w[i / (D / 2)][i % (D / 2)] = reinterpret_cast<const uint32_t *>(norm_w)[i];
 
-    const int rows_per_tok = 2 * H;
+    const int nq = q_in ? H : 0;                        // q rows per token (0 = q left out)
+    const int rows_per_tok = nq + (k_in ? H : 0);
     for (int64_t t0 = (int64_t)blockIdx.x * kTokensPerIter; t0 < T; t0 += (int64_t)gridDim.x * kTokensPerIter) {
         __syncthreads();                                // previous iteration done with s_cos/s_sin
         const int ntok = (int)(T - t0 < kTokensPerIter ? T - t0 : kTokensPerIter);
@@ -128,8 +135,8 @@ qk_norm_rope_kernel(const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out,
                 const bool row_ok = r < nrows;
                 const int tt = row_ok ? r / rows_per_tok : 0;
                 const int rem = row_ok ? r % rows_per_tok : 0;
-                const int which = rem >= H;             // 0 = q, 1 = k
-                const int h = rem - which * H;
+                const int which = rem >= nq;            // 0 = q, 1 = k
+                const int h = rem - which * nq;
                 const int64_t t = t0 + tt;
                 act[k] = row_ok && c < CHUNKS;
                 tt_[k] = tt;
@@ -168,18 +175,38 @@ qk_norm_rope_kernel(const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out,
                     }
                 }
                 if (act[k]) {
-                    const float4 *cs_ = s_cs[tt_[k]] + c * 4;
                     uint32_t oa[4], ob[4];
+                    if constexpr (!IL) {
+                        const float4 *cs_ = s_cs[tt_[k]] + c * 4;
 #pragma unroll
-                    for (int i = 0; i < 8; i += 2) {
-                        const float4 t = cs_[i / 2];
-                        const uint64_t cc = f2(t.x, t.y), sn = f2(t.z, t.w);
-                        const uint64_t a = f2(xa[i], xa[i + 1]), b = f2(xb[i], xb[i + 1]);
-                        float ya0, ya1, yb0, yb1;
-                        f2_split(f2_sub(f2_mul(a, cc), f2_mul(b, sn)), ya0, ya1);     // x cos - x' sin
-                        f2_split(f2_fma(a, sn, f2_mul(b, cc)), yb0, yb1);             // x' cos + x sin
-                        oa[i / 2] = pack2(ya0, ya1);
-                        ob[i / 2] = pack2(yb0, yb1);
+                        for (int i = 0; i < 8; i += 2) {
+                            const float4 t = cs_[i / 2];
+                            const uint64_t cc = f2(t.x, t.y), sn = f2(t.z, t.w);
+                            const uint64_t a = f2(xa[i], xa[i + 1]), b = f2(xb[i], xb[i + 1]);
+                            float ya0, ya1, yb0, yb1;
+                            f2_split(f2_sub(f2_mul(a, cc), f2_mul(b, sn)), ya0, ya1);     // x cos - x' sin
+                            f2_split(f2_fma(a, sn, f2_mul(b, cc)), yb0, yb1);             // x' cos + x sin
+                            oa[i / 2] = pack2(ya0, ya1);
+                            ob[i / 2] = pack2(yb0, yb1);
+                        }
+                    } else {
+                        // chunk c of the first half holds pairs 4c..4c+3, the second half's chunk c
+                        // pairs D/4 + 4c .. D/4 + 4c + 3 (D/4 is even, so both start a float4 entry)
+                        const float4 *csa = s_cs[tt_[k]] + 2 * c, *csb = s_cs[tt_[k]] + D / 8 + 2 * c;
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) {
+                            const float4 ta = csa[p >> 1], tb = csb[p >> 1];
+                            const float ca = (p & 1) ? ta.y : ta.x, sa = (p & 1) ? ta.w : ta.z;
+                            const float cb = (p & 1) ? tb.y : tb.x, sb = (p & 1) ? tb.w : tb.z;
+                            float y0, y1;
+                            // (x0 cos - x1 sin, x1 cos + x0 sin) = (x0, x1) * cos + (x1, x0) * (-sin, sin)
+                            f2_split(f2_fma(f2(xa[2 * p + 1], xa[2 * p]), f2(-sa, sa),
+                                            f2_mul(f2(xa[2 * p], xa[2 * p + 1]), f2(ca, ca))), y0, y1);
+                            oa[p] = pack2(y0, y1);
+                            f2_split(f2_fma(f2(xb[2 * p + 1], xb[2 * p]), f2(-sb, sb),
+                                            f2_mul(f2(xb[2 * p], xb[2 * p + 1]), f2(cb, cb))), y0, y1);
+                            ob[p] = pack2(y0, y1);
+                        }
                     }
                     *reinterpret_cast<uint4 *>(dst[k]) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
                     *reinterpret_cast<uint4 *>(dst[k] + HALF) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
@@ -192,14 +219,16 @@ qk_norm_rope_kernel(const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out,
 template <int D>
 cudaError_t launch_d(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T, int H,
                      int64_t qis, int64_t qos, int64_t kis, int64_t kos, const int32_t *pos_hw,
-                     const float *inv_freq, const void *norm_w, float eps, int num_sms, cudaStream_t stream)
+                     const float *inv_freq, const void *norm_w, float eps, bool interleaved, int num_sms,
+                     cudaStream_t stream)
 {
     const int64_t want = (T + kTokensPerIter - 1) / kTokensPerIter;
     const int64_t cap = (int64_t)num_sms * 8;
     const unsigned blocks = (unsigned)(want < cap ? want : cap);
     if (blocks == 0) return cudaSuccess;
     LaunchScope scope("qk_norm_rope", stream);
-    qk_norm_rope_kernel<D><<<blocks, kThreads, 0, stream>>>(
+    auto kern = interleaved ? qk_norm_rope_kernel<D, true> : qk_norm_rope_kernel<D, false>;
+    kern<<<blocks, kThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(q_in), static_cast<__nv_bfloat16 *>(q_out),
         static_cast<const __nv_bfloat16 *>(k_in), static_cast<__nv_bfloat16 *>(k_out), T, H, qis, qos, kis, kos,
         reinterpret_cast<const int2 *>(pos_hw), inv_freq, static_cast<const __nv_bfloat16 *>(norm_w), eps);
@@ -211,13 +240,13 @@ cudaError_t launch_d(const void *q_in, void *q_out, const void *k_in, void *k_ou
 cudaError_t launch_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T,
                                 int H, int D, int64_t q_in_stride, int64_t q_out_stride,
                                 int64_t k_in_stride, int64_t k_out_stride, const int32_t *pos_hw,
-                                const float *inv_freq, const void *norm_w, float eps, int num_sms,
-                                cudaStream_t stream)
+                                const float *inv_freq, const void *norm_w, float eps, bool interleaved,
+                                int num_sms, cudaStream_t stream)
 {
 #define VIT_QKNR(DD)                                                                                   \
     case DD:                                                                                           \
         return launch_d<DD>(q_in, q_out, k_in, k_out, T, H, q_in_stride, q_out_stride, k_in_stride,   \
-                            k_out_stride, pos_hw, inv_freq, norm_w, eps, num_sms, stream);
+                            k_out_stride, pos_hw, inv_freq, norm_w, eps, interleaved, num_sms, stream);
     switch (D) {
         VIT_QKNR(32)
         VIT_QKNR(64)
