@@ -132,9 +132,11 @@ class ClockSampler:
 class Path:
     """Device-resident buffers and the three calls of one step."""
 
-    def __init__(self, vit, w: wl.Workload, t: dict, device, lse: bool = False, interleaved: bool = False):
+    def __init__(self, vit, w: wl.Workload, t: dict, device, lse: bool = False, interleaved: bool = False,
+                 fused_q: bool = False):
         self.vit, self.w = vit, w
-        self.interleaved = interleaved
+        self.interleaved, self.fused_q = interleaved, fused_q
+        self.max_pos = int(w.grid_hw.max())
         T, H, D, B = w.total_tokens, w.heads, w.head_dim, w.num_segments
         self.grid = torch.from_numpy(w.grid_hw.copy()).to(device)
         self.q, self.k, self.v = (t[n].to(device) for n in ("q", "k", "v"))
@@ -149,22 +151,33 @@ class Path:
     def step(self):
         vit, w = self.vit, self.w
         inv_freq, pos, cu = vit.rope_freqs(self.grid, w.total_tokens, w.head_dim, w.theta, status=self.status)
+        if self.fused_q:
+            # position table, K pre-stage, attention that normalises and rotates Q as it loads it
+            cs = vit.rope_table(inv_freq, w.head_dim, self.max_pos)
+            vit.encoder_attn(self.q, self.k, self.v, cu, w.max_seqlen, pos, inv_freq, cs, self.nw, w.eps,
+                             interleaved=self.interleaved, k_out=self.kr, out=self.out, workspace=self.ws,
+                             status=self.status, lse=self.lse)
+            return
         vit.qk_norm_rope(self.q, self.k, pos, inv_freq, self.nw, w.eps, q_out=self.qr, k_out=self.kr,
                          interleaved=self.interleaved)
         vit.varlen_attn(self.qr, self.kr, self.v, cu, w.max_seqlen, out=self.out, workspace=self.ws,
                         status=self.status, lse=self.lse)
 
 
-def e2e_step(vit, w, host, device, stream):
-    """Through the public API from pinned host buffers: H2D inputs, the three calls, D2H output."""
+def e2e_step(vit, w, host, device, stream, fused_q=False):
+    """Through the public API from pinned host buffers: H2D inputs, the calls, D2H output."""
     grid = host["grid"].to(device, non_blocking=True)
     q = host["q"].to(device, non_blocking=True)
     k = host["k"].to(device, non_blocking=True)
     v = host["v"].to(device, non_blocking=True)
     nw = host["nw"].to(device, non_blocking=True) if host["nw"] is not None else None
     inv_freq, pos, cu = vit.rope_freqs(grid, w.total_tokens, w.head_dim, w.theta)
-    qr, kr = vit.qk_norm_rope(q, k, pos, inv_freq, nw, w.eps, inplace=True)
-    out = vit.varlen_attn(qr, kr, v, cu, w.max_seqlen)
+    if fused_q:
+        cs = vit.rope_table(inv_freq, w.head_dim, int(w.grid_hw.max()))
+        out = vit.encoder_attn(q, k, v, cu, w.max_seqlen, pos, inv_freq, cs, nw, w.eps, k_out=k)
+    else:
+        qr, kr = vit.qk_norm_rope(q, k, pos, inv_freq, nw, w.eps, inplace=True)
+        out = vit.varlen_attn(qr, kr, v, cu, w.max_seqlen)
     host["out"].copy_(out, non_blocking=True)
 
 
@@ -237,7 +250,7 @@ def run_ours(args, rank, world, local):
     w = wl.make_config(args.config)
     t = w.tensors()
     T, H, D = w.total_tokens, w.heads, w.head_dim
-    path = Path(vit, w, t, device, lse=args.lse, interleaved=args.interleaved)
+    path = Path(vit, w, t, device, lse=args.lse, interleaved=args.interleaved, fused_q=args.fused_q)
     stream = torch.cuda.current_stream()
     tensor_bytes = T * H * D * 2
     working_set = 6 * tensor_bytes
@@ -298,14 +311,14 @@ def run_ours(args, rank, world, local):
         h2d = 3 * tensor_bytes + host["grid"].numel() * 4 + (host["nw"].numel() * 2 if host["nw"] is not None else 0)
         d2h = tensor_bytes
         for _ in range(2):
-            e2e_step(vit, w, host, device, stream)
+            e2e_step(vit, w, host, device, stream, args.fused_q)
         torch.cuda.synchronize()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e2e_steps = max(1, min(args.steps, 10))
         e0.record(stream)
         for _ in range(e2e_steps):
-            e2e_step(vit, w, host, device, stream)
+            e2e_step(vit, w, host, device, stream, args.fused_q)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, device)
@@ -337,8 +350,8 @@ def run_ours(args, rank, world, local):
             if dom == "attn_short":      # q, k, v read and out written once per token it owns
                 L = w.lengths
                 alg = 8.0 * float(L[L <= short_max].sum()) * H * D
-            elif dom == "qk_norm_rope":  # q and k read and written once
-                alg = 8.0 * T * H * D
+            elif dom == "qk_norm_rope":  # q and k (k alone with --fused-q) read and written once
+                alg = (4.0 if args.fused_q else 8.0) * T * H * D
             else:
                 alg = 8.0 * T
             achieved = alg / avg_s / 1e9
@@ -352,6 +365,7 @@ def run_ours(args, rank, world, local):
         "config": {"workload": w.name, "tokens": T, "segments": w.num_segments, "heads": H, "head_dim": D,
                    "qk_norm": w.qk_norm, "max_seqlen": w.max_seqlen, "useful_flops_per_step": flops,
                    "rope": "interleaved" if args.interleaved else "rotate_half", "lse": bool(args.lse),
+                   "q_prologue": "fused into the attention Q load" if args.fused_q else "separate pass",
                    "l2": "L2 flushed between steps" if flush else
                    f"inputs larger than L2 ({working_set / 2 ** 20:.0f} MiB working set)",
                    "parallelism": "replicas" if world > 1 else "single"},
@@ -461,6 +475,8 @@ def main():
                     help="segments longer than this run on the tcgen05 kernel (library default 64)")
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--lse", action="store_true", help="also write the per-row log-sum-exp [T, H] each step")
+    ap.add_argument("--fused-q", action="store_true",
+                    help="normalise and rotate Q inside the attention kernels (K alone in the pre-stage)")
     ap.add_argument("--interleaved", action="store_true",
                     help="rotate adjacent pairs (the complex_rope mode) instead of (m, m + D/2)")
     args = ap.parse_args()

@@ -62,7 +62,8 @@ enum {
     VIT_ERR_SEQLEN_EXCEEDS_MAX = -11,/* device: some segment longer than max_seqlen */
     VIT_ERR_GRID_MISMATCH = -12,     /* device: sum of h*w over the grid != T, or h, w < 0 */
     VIT_ERR_TIMEOUT = -13,           /* device: a bounded wait inside a kernel gave up */
-    VIT_ERR_BAD_ARGUMENT = -14       /* any other invalid scalar argument */
+    VIT_ERR_BAD_ARGUMENT = -14,      /* any other invalid scalar argument */
+    VIT_ERR_POSITION_RANGE = -15     /* device: a token position lies outside the rope table */
 };
 
 #define VIT_MAX_SEGMENTS 8192
@@ -168,6 +169,28 @@ vit_status_t vit_qk_norm_rope_ex(const void *q_in, void *q_out, const void *k_in
                                  const void *norm_w, float eps, int rope_mode, vit_stream_t stream);
 
 /*
+ * Rotary cos/sin table over positions, for the attention call that rotates Q
+ * itself (vit_varlen_attn_fused_q).
+ *
+ * [Dots] VisionRotaryEmbedding builds freqs = outer(arange(max_grid_size),
+ * inv_freq) once and the tower indexes it by each patch's (row, col). Same
+ * here, with cos and sin already taken:
+ *   cos_sin[p][f/2] = {cos a, cos a', sin a, sin a'},  a = p * inv_freq[f],
+ *                     a' = p * inv_freq[f + 1],  f = 0, 2, .., D/4 - 2,
+ * in fp32, the same product and sincosf the prologue evaluates per token, so
+ * both paths rotate with the same bits.
+ *
+ *   inv_freq   device fp32 [head_dim/4] from vit_rope_freqs(dim = head_dim/2).
+ *   head_dim   D, one of {32, 64, 80, 96, 128}.
+ *   max_pos    number of positions, >= 1: larger than every row and column
+ *              index a token will have (max over images of max(h, w)).
+ *   cos_sin    device fp32 output of max_pos * head_dim/2 floats, 16-byte
+ *              aligned.
+ */
+vit_status_t vit_rope_table(const float *inv_freq, int head_dim, int max_pos, float *cos_sin,
+                            vit_stream_t stream);
+
+/*
  * Workspace bytes vit_varlen_attn needs for these sizes (an upper bound
  * independent of the segment lengths). Returns 0 for invalid sizes.
  */
@@ -224,6 +247,40 @@ vit_status_t vit_varlen_attn_lse(const void *q, const void *k, const void *v, in
                                  void *out, int64_t out_stride, float *lse,
                                  void *workspace, size_t workspace_bytes,
                                  int32_t *status_dev, vit_stream_t stream);
+
+/* How vit_varlen_attn_fused_q normalises and rotates Q (all pointers device). */
+typedef struct vit_q_rope {
+    const int32_t *pos_hw;   /* int32 [T, 2] (row, col) of every token, from vit_rope_freqs */
+    const float *cos_sin;    /* table from vit_rope_table(inv_freq, D, max_pos, .) */
+    int max_pos;             /* positions in the table */
+    const void *norm_w;      /* bf16 [D] q weight (row 0 of the prologue's [2, D]), 16-byte
+                                aligned, or NULL for no QK-norm */
+    float eps;               /* RMSNorm epsilon, >= 0 */
+    int rope_mode;           /* VIT_ROPE_ROTATE_HALF or VIT_ROPE_INTERLEAVED */
+} vit_q_rope_t;
+
+/*
+ * vit_varlen_attn_lse with the Q half of the prologue fused into the kernels'
+ * Q load: `q` holds the raw projections, and every Q tile is normalised and
+ * rotated in shared memory after it arrives, before its first product. K must
+ * already be normalised and rotated (vit_qk_norm_rope_ex with the q half left
+ * out: a one-tensor pre-stage). This removes one write and one read of q from
+ * HBM; the result is bit-identical to running vit_qk_norm_rope_ex on q and k
+ * and then vit_varlen_attn_lse.
+ *
+ * Arguments as for vit_varlen_attn_lse, plus:
+ *   q_rope   host pointer to the Q normalisation and rotation (see above).
+ * Device-detected: a token whose row or column is outside [0, max_pos)
+ * stores VIT_ERR_POSITION_RANGE; the table is never read out of range, but
+ * the outputs of such a call are undefined.
+ */
+vit_status_t vit_varlen_attn_fused_q(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                     int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                                     const vit_q_rope_t *q_rope,
+                                     const int32_t *cu_seqlens, int B, int max_seqlen, float scale,
+                                     void *out, int64_t out_stride, float *lse,
+                                     void *workspace, size_t workspace_bytes,
+                                     int32_t *status_dev, vit_stream_t stream);
 
 /* Size of the fixed device scratch array behind vit_varlen_attn_noalloc (per GPU). */
 #define VIT_NOALLOC_WORKSPACE_BYTES (4u << 20)

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_status_strings(L):
     assert vit.status_string(0) == "ok"
-    for code in range(-1, -15, -1):
+    for code in range(-1, -16, -1):
         s = vit.status_string(code)
         assert s and s != "unknown status", code
     assert vit.status_string(-999) == "unknown status"
@@ -126,6 +126,27 @@ def test_extended_calls_validation_without_gpu(L):
     args_bad = list(args)
     args_bad[5] = 81
     assert L.vit_varlen_attn_lse(*args_bad, p(16), p(256), 1 << 20, None, None) == -2
+
+
+def test_fused_q_and_table_validation_without_gpu(L):
+    p = ctypes.c_void_p
+    assert L.vit_rope_table(p(16), 81, 10, p(16), None) == -2
+    assert L.vit_rope_table(p(16), 80, 0, p(16), None) == -14
+    assert L.vit_rope_table(None, 80, 10, p(16), None) == -1
+    assert L.vit_rope_table(p(16), 80, 10, p(24), None) == -5
+
+    def fused(qr):
+        return L.vit_varlen_attn_fused_q(p(16), p(16), p(16), 128, 2, 80, 160, 160, 160,
+                                         None if qr is None else ctypes.byref(qr), p(16), 1, 128, 0.0, p(16), 160,
+                                         None, p(256), 1 << 20, None, None)
+    QR = vit._QRope
+    assert fused(None) == -1
+    assert fused(QR(16, 16, 64, None, 1e-6, 2)) == -14          # unknown rotary pairing
+    assert fused(QR(16, 16, 0, None, 1e-6, 0)) == -14           # empty table
+    assert fused(QR(16, 16, 64, None, -1.0, 0)) == -14          # eps < 0
+    assert fused(QR(None, 16, 64, None, 1e-6, 0)) == -1
+    assert fused(QR(16, 24, 64, None, 1e-6, 0)) == -5           # table not 16-byte aligned
+    assert fused(QR(16, 16, 64, 18, 1e-6, 0)) == -5             # weight not 16-byte aligned
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -33,6 +33,11 @@ class VitError(RuntimeError):
         super().__init__(f"{what}: {status_string(code)} (status {code})")
 
 
+class _QRope(ctypes.Structure):
+    _fields_ = [("pos_hw", ctypes.c_void_p), ("cos_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int),
+                ("norm_w", ctypes.c_void_p), ("eps", ctypes.c_float), ("rope_mode", ctypes.c_int)]
+
+
 class _KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
 
@@ -61,6 +66,9 @@ def lib() -> ctypes.CDLL:
                                           sz, vp, vp]
             L.vit_varlen_attn_lse.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, vp, i32, i32, f32, vp, i64,
                                               vp, vp, sz, vp, vp]
+            L.vit_varlen_attn_fused_q.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, ctypes.POINTER(_QRope),
+                                                  vp, i32, i32, f32, vp, i64, vp, vp, sz, vp, vp]
+            L.vit_rope_table.argtypes = [vp, i32, i32, vp, vp]
             L.vit_read_status.argtypes = [vp, vp]
             L.vit_set_short_segment_max.argtypes = [i32]
             L.vit_set_short_segment_max.restype = i32
@@ -70,8 +78,8 @@ def lib() -> ctypes.CDLL:
             L.vit_kernel_timing.argtypes = [i32]
             L.vit_kernel_timing_read.argtypes = [ctypes.POINTER(_KernelTime), i32]
             for fn in ("vit_device_supported", "vit_rope_freqs", "vit_qk_norm_rope", "vit_qk_norm_rope_ex",
-                       "vit_varlen_attn", "vit_varlen_attn_lse", "vit_read_status", "vit_kernel_timing",
-                       "vit_kernel_timing_read"):
+                       "vit_varlen_attn", "vit_varlen_attn_lse", "vit_varlen_attn_fused_q", "vit_rope_table",
+                       "vit_read_status", "vit_kernel_timing", "vit_kernel_timing_read"):
                 getattr(L, fn).restype = i32
             _lib = L
     return _lib
@@ -134,6 +142,17 @@ def rope_freqs(grid_hw: torch.Tensor, total_tokens: int, head_dim: int, theta: f
     _check(lib().vit_rope_freqs(dim, float(theta), _ptr(grid_hw), n, int(total_tokens), _ptr(inv_freq), _ptr(pos),
                                 _ptr(cu), _ptr(status), _stream(stream)), "vit_rope_freqs")
     return inv_freq, pos, cu
+
+
+def rope_table(inv_freq: torch.Tensor, head_dim: int, max_pos: int, *, stream=None) -> torch.Tensor:
+    """cos/sin of p * inv_freq for positions p < max_pos (fp32 [max_pos, head_dim/2]), the table the
+    fused-Q attention rotates with."""
+    if inv_freq.dtype != torch.float32 or not inv_freq.is_cuda or inv_freq.numel() != head_dim // 4:
+        raise ValueError(f"inv_freq must be a CUDA float32 tensor [{head_dim // 4}]")
+    cs = torch.empty((int(max_pos), head_dim // 2), dtype=torch.float32, device=inv_freq.device)
+    _check(lib().vit_rope_table(_ptr(inv_freq), int(head_dim), int(max_pos), _ptr(cs), _stream(stream)),
+           "vit_rope_table")
+    return cs
 
 
 ROPE_ROTATE_HALF = 0    # pairs (m, m + D/2)
@@ -219,6 +238,65 @@ def varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: t
                                      int(max_seqlen), sc, _ptr(out), os_, _ptr(lse), _ptr(workspace), ws_bytes,
                                      _ptr(status), _stream(stream)), "vit_varlen_attn_lse")
     return out, lse
+
+
+def varlen_attn_fused_q(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor | None,
+                        max_seqlen: int, pos_hw: torch.Tensor, cos_sin: torch.Tensor,
+                        q_norm_w: torch.Tensor | None = None, eps: float = 1e-6, scale: float | None = None, *,
+                        interleaved: bool = False, num_segments: int | None = None,
+                        out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        status: torch.Tensor | None = None, return_lse: bool = False,
+                        lse: torch.Tensor | None = None, stream=None):
+    """varlen_attn on raw q: the kernels normalise (q_norm_w [D], or None) and rotate every Q tile
+    after loading it. k must already be normalised and rotated (qk_norm_rope(None, k, ...))."""
+    T, H, D = q.shape
+    qs, ks, vs = _tok_stride(q, "q", H, D), _tok_stride(k, "k", H, D), _tok_stride(v, "v", H, D)
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or not cu_seqlens.is_contiguous():
+            raise ValueError("cu_seqlens must be a contiguous CUDA int32 tensor [B + 1]")
+        B = cu_seqlens.numel() - 1
+    else:
+        if num_segments is None:
+            raise ValueError("num_segments is required when cu_seqlens is None")
+        B = int(num_segments)
+    if cos_sin.dtype != torch.float32 or cos_sin.dim() != 2 or cos_sin.shape[1] != D // 2 \
+            or not cos_sin.is_contiguous():
+        raise ValueError(f"cos_sin must be the contiguous float32 [max_pos, {D // 2}] table of rope_table")
+    if q_norm_w is not None and (q_norm_w.dtype != torch.bfloat16 or q_norm_w.numel() != D
+                                 or not q_norm_w.is_contiguous()):
+        raise ValueError("q_norm_w must be a contiguous bfloat16 tensor [D]")
+    if out is None:
+        out = torch.empty((T, H, D), dtype=q.dtype, device=q.device)
+    os_ = _tok_stride(out, "out", H, D)
+    if workspace is None:
+        workspace = torch.empty(max(workspace_size(T, H, B, D), 16), dtype=torch.uint8, device=q.device)
+    if return_lse and lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (T, H) or not lse.is_contiguous()):
+        raise ValueError(f"lse must be a contiguous CUDA float32 tensor [{T}, {H}]")
+    qr = _QRope(pos_hw.data_ptr(), cos_sin.data_ptr(), int(cos_sin.shape[0]),
+                q_norm_w.data_ptr() if q_norm_w is not None else None, float(eps),
+                ROPE_INTERLEAVED if interleaved else ROPE_ROTATE_HALF)
+    _check(lib().vit_varlen_attn_fused_q(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, ctypes.byref(qr),
+                                         _ptr(cu_seqlens), B, int(max_seqlen),
+                                         float(scale) if scale is not None else 0.0, _ptr(out), os_, _ptr(lse),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _ptr(status), _stream(stream)), "vit_varlen_attn_fused_q")
+    return (out, lse) if lse is not None else out
+
+
+def encoder_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen: int,
+                 pos_hw: torch.Tensor, inv_freq: torch.Tensor, cos_sin: torch.Tensor,
+                 norm_w: torch.Tensor | None = None, eps: float = 1e-6, *, interleaved: bool = False,
+                 k_out: torch.Tensor | None = None, **kw):
+    """The whole hot path with the Q prologue fused into attention: a one-tensor K pre-stage
+    (norm_w row 1, written to k_out, or in place when k_out is k), then attention on raw q with
+    norm_w row 0 applied as Q tiles load."""
+    _, kr = qk_norm_rope(None, k, pos_hw, inv_freq, norm_w, eps, k_out=k_out, interleaved=interleaved,
+                         stream=kw.get("stream"))
+    q_w = norm_w.reshape(2, -1)[0] if norm_w is not None else None
+    return varlen_attn_fused_q(q, kr, v, cu_seqlens, max_seqlen, pos_hw, cos_sin, q_w, eps,
+                               interleaved=interleaved, **kw)
 
 
 def set_short_segment_max(short_max: int) -> int:

@@ -84,6 +84,7 @@ const char *vit_status_string(vit_status_t s)
         case VIT_ERR_GRID_MISMATCH: return "patch grid does not sum to T (or has negative sides)";
         case VIT_ERR_TIMEOUT: return "a bounded device-side wait expired";
         case VIT_ERR_BAD_ARGUMENT: return "invalid argument";
+        case VIT_ERR_POSITION_RANGE: return "a token position lies outside the rope table";
         default: return "unknown status";
     }
 }
@@ -154,6 +155,17 @@ vit_status_t vit_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, v
                                k_out_stride, pos_hw, inv_freq, norm_w, eps, VIT_ROPE_ROTATE_HALF, stream);
 }
 
+vit_status_t vit_rope_table(const float *inv_freq, int head_dim, int max_pos, float *cos_sin, vit_stream_t stream)
+{
+    if (!head_dim_ok(head_dim)) return VIT_ERR_BAD_HEAD_DIM;
+    if (max_pos < 1) return VIT_ERR_BAD_ARGUMENT;
+    if (!inv_freq || !cos_sin) return VIT_ERR_NULL_POINTER;
+    if (((uintptr_t)inv_freq & 3u) || !aligned16(cos_sin)) return VIT_ERR_MISALIGNED;
+    vit_status_t st = device_info(nullptr);
+    if (st != VIT_OK) return st;
+    return from_cuda(launch_rope_table(inv_freq, head_dim / 4, max_pos, cos_sin, (cudaStream_t)stream));
+}
+
 size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D)
 {
     if (T < 0 || T >= kMaxTokens || H < 1 || B < 0 || B > VIT_MAX_SEGMENTS || !head_dim_ok(D)) return 0;
@@ -163,10 +175,15 @@ size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D)
     return sizeof(WsHeader) + sizeof(Item) * (size_t)items;
 }
 
-vit_status_t vit_varlen_attn_lse(const void *q, const void *k, const void *v, int64_t T, int H, int D,
-                                 int64_t q_stride, int64_t k_stride, int64_t v_stride, const int32_t *cu_seqlens,
-                                 int B, int max_seqlen, float scale, void *out, int64_t out_stride, float *lse,
-                                 void *workspace, size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
+}  // extern "C"
+
+namespace {
+
+vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64_t T, int H, int D, int64_t q_stride,
+                              int64_t k_stride, int64_t v_stride, const vit_q_rope_t *q_rope,
+                              const int32_t *cu_seqlens, int B, int max_seqlen, float scale, void *out,
+                              int64_t out_stride, float *lse, void *workspace, size_t workspace_bytes,
+                              int32_t *status_dev, vit_stream_t stream)
 {
     if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
     if (T < 0 || T >= kMaxTokens || H < 1 || B < 0) return VIT_ERR_BAD_SHAPE;
@@ -182,6 +199,15 @@ vit_status_t vit_varlen_attn_lse(const void *q, const void *k, const void *v, in
             return VIT_ERR_BAD_STRIDE;
         if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return VIT_ERR_MISALIGNED;
         if ((uintptr_t)lse & 3u) return VIT_ERR_MISALIGNED;
+    }
+    if (q_rope && T > 0) {
+        if (!q_rope->pos_hw || !q_rope->cos_sin) return VIT_ERR_NULL_POINTER;
+        if (q_rope->max_pos < 1) return VIT_ERR_BAD_ARGUMENT;
+        if (!(q_rope->eps >= 0.f) || !isfinite(q_rope->eps)) return VIT_ERR_BAD_ARGUMENT;
+        if (q_rope->rope_mode != VIT_ROPE_ROTATE_HALF && q_rope->rope_mode != VIT_ROPE_INTERLEAVED)
+            return VIT_ERR_BAD_ARGUMENT;
+        if (((uintptr_t)q_rope->pos_hw & 7u) || !aligned16(q_rope->cos_sin) || !aligned16(q_rope->norm_w))
+            return VIT_ERR_MISALIGNED;
     }
     if (!workspace) return VIT_ERR_NULL_POINTER;
     if (!aligned16(workspace) || ((uintptr_t)cu_seqlens & 3u)) return VIT_ERR_MISALIGNED;
@@ -221,6 +247,17 @@ vit_status_t vit_varlen_attn_lse(const void *q, const void *k, const void *v, in
     a.hdr = hdr;
     a.items = items;
     a.status = status_dev;
+    a.fuse_q = q_rope != nullptr;
+    a.qr = rope::QRope{};
+    if (q_rope) {
+        a.qr.pos_hw = reinterpret_cast<const int2 *>(q_rope->pos_hw);
+        a.qr.cos_sin = reinterpret_cast<const float4 *>(q_rope->cos_sin);
+        a.qr.norm_w = static_cast<const uint4 *>(q_rope->norm_w);
+        a.qr.max_pos = q_rope->max_pos;
+        a.qr.eps = q_rope->eps;
+        a.qr.interleaved = q_rope->rope_mode == VIT_ROPE_INTERLEAVED;
+        a.qr.status = status_dev;
+    }
     // a segment can only be long when the bound allows it
     const int64_t longest = cu_seqlens ? (int64_t)max_seqlen : T / B;
     if (longest > sp.short_max) {
@@ -229,6 +266,30 @@ vit_status_t vit_varlen_attn_lse(const void *q, const void *k, const void *v, in
     }
     if (sp.short_max > 0) e = launch_attn_short(a, max_items(T, H, B, sp.bm_short), sms, s);
     return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+vit_status_t vit_varlen_attn_lse(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                 int64_t q_stride, int64_t k_stride, int64_t v_stride, const int32_t *cu_seqlens,
+                                 int B, int max_seqlen, float scale, void *out, int64_t out_stride, float *lse,
+                                 void *workspace, size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
+{
+    return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, nullptr, cu_seqlens, B, max_seqlen,
+                            scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
+}
+
+vit_status_t vit_varlen_attn_fused_q(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                     int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                                     const vit_q_rope_t *q_rope, const int32_t *cu_seqlens, int B, int max_seqlen,
+                                     float scale, void *out, int64_t out_stride, float *lse, void *workspace,
+                                     size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
+{
+    if (!q_rope) return VIT_ERR_NULL_POINTER;
+    return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, q_rope, cu_seqlens, B, max_seqlen,
+                            scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
 }
 
 vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_t T, int H, int D, int64_t q_stride,

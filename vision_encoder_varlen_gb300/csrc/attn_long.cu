@@ -20,7 +20,10 @@
 //                 O_i += P V        (TS MMA, A=P from TMEM, B=V MN-major)
 //               each issuer orders QK(j+1) before PV(j), so S of the next key
 //               tile is computed while its softmax group turns S into P.
-//   warp 3      idle (completes the control warpgroup)
+//   warp 3      idle (completes the control warpgroup); when Q arrives raw, it
+//               normalises and rotates each Q pair in shared memory between
+//               the TMA landing and the first MMA (fence to the async proxy,
+//               then q_ready), one row per lane at a time
 //   warps 4-7   softmax group 0 (tile 0), one TMEM lane = one query row per
 //   warps 8-11  softmax group 1 (tile 1)  thread: row max, lazy rescaling of
 //               O (only when the max grows by more than 2^8), exp2 with the
@@ -80,7 +83,7 @@ template <int D> struct LongCfg {
 };
 
 struct Bars {
-    uint64_t q_full[2], q_empty[2];
+    uint64_t q_full[2], q_empty[2], q_ready[2];
     uint64_t k_full[3], v_full[3], kv_empty[3];
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
     uint64_t drain[2];
@@ -88,12 +91,12 @@ struct Bars {
 
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_addr(&b); }
 
-template <int D, bool LSE>
+template <int D, bool LSE, bool FQ>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out, int64_t out_stride,
                  float *__restrict__ lse, int H, float scale_log2, const WsHeader *__restrict__ hdr,
-                 const Item *__restrict__ items, int32_t *status, int stall_v)
+                 const Item *__restrict__ items, int32_t *status, int stall_v, const rope::QRope qr)
 {
     using C = LongCfg<D>;
     constexpr int BN = C::BN, ST = C::STAGES, NSLAB = C::NSLAB;
@@ -111,6 +114,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_addr(bars.q_full[b]), 1);
             mbar_init(bar_addr(bars.q_empty[b]), 2);     // one commit from each MMA issuer
+            mbar_init(bar_addr(bars.q_ready[b]), 1);     // warp 3 after rotating raw Q
         }
         for (int s = 0; s < ST; ++s) {
             mbar_init(bar_addr(bars.k_full[s]), 1);
@@ -166,6 +170,17 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // two bits per stage, kept in registers
             uint32_t q_pend = 0, k_pend = 0, v_pend = 0;     // q_pend: two bits per Q buffer
             bool ok = true;
+            auto load_q = [&](uint32_t qb, uint32_t qn, int q0, int head) {
+                mbar_arrive_expect_tx(bar_addr(bars.q_full[qb]), 2 * C::Q_TILE);
+                for (int i = 0; i < 2; ++i)
+                    for (int s = 0; s < NSLAB; ++s)
+                        tma_load_2d(smem_addr(base + C::OFF_Q + (2 * qb + i) * C::Q_TILE + s * C::Q_SLAB), &tm_q,
+                                    head * D + 16 * s, q0 + BM * i, bar_addr(bars.q_full[qb]));
+                q_pend = (q_pend & ~(3u << (2 * qb))) | (((qn & 1) + 1) << (2 * qb));
+            };
+            // raw Q needs time for warp 3 to rotate it, so with two Q buffers the next item's Q
+            // goes out as soon as its buffer is free rather than after this item's last K/V tile
+            bool q_early = false;                            // Q of item q_it already issued
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++q_it) {
                 const Item item = items[it];
                 const int seg0 = item.x, seg_len = item.y, q0 = item.z, head = item.w;
@@ -173,14 +188,23 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // Q pairs alternate between two buffers, so the next item's Q is loaded while
                 // the current item still runs
                 const uint32_t qb = q_it % C::QBUF, qn = q_it / C::QBUF;   // buffer, its use count
-                if (qn > 0 && !(ok = wait(bars.q_empty[qb], (qn - 1) & 1))) break;
-                mbar_arrive_expect_tx(bar_addr(bars.q_full[qb]), 2 * C::Q_TILE);
-                for (int i = 0; i < 2; ++i)
-                    for (int s = 0; s < NSLAB; ++s)
-                        tma_load_2d(smem_addr(base + C::OFF_Q + (2 * qb + i) * C::Q_TILE + s * C::Q_SLAB), &tm_q,
-                                    head * D + 16 * s, q0 + BM * i, bar_addr(bars.q_full[qb]));
-                q_pend = (q_pend & ~(3u << (2 * qb))) | (((qn & 1) + 1) << (2 * qb));
+                if (!q_early) {
+                    if (qn > 0 && !(ok = wait(bars.q_empty[qb], (qn - 1) & 1))) break;
+                    load_q(qb, qn, q0, head);
+                }
+                q_early = false;
+                const int it_next = it + (int)gridDim.x;
                 for (int j = 0; j < n_kv; ++j, ++g) {
+                    if constexpr (FQ && C::QBUF == 2) {
+                        if (!q_early && it_next < n_items) {
+                            const uint32_t qb1 = (q_it + 1) & 1, qn1 = (q_it + 1) >> 1;
+                            if (qn1 == 0 || mbar_test(bar_addr(bars.q_empty[qb1]), (qn1 - 1) & 1)) {
+                                const Item nx = items[it_next];
+                                load_q(qb1, qn1, nx.z, nx.w);
+                                q_early = true;
+                            }
+                        }
+                    }
                     const int st = g % ST;
                     if (g >= (uint32_t)ST && !(ok = wait(bars.kv_empty[st], (g / ST - 1) & 1))) break;
                     const int row = seg0 + j * BN;
@@ -260,7 +284,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 uint32_t st = t % ST, ph = (t / ST) & 1;
                 const uint32_t qb = item_cnt % C::QBUF;         // Q buffer of this item
                 const uint64_t dq = dq_base + qb * ((2 * C::Q_TILE) >> 4);
-                if (!(ok = wait(bars.q_full[qb], (item_cnt / C::QBUF) & 1))) break;
+                if (!(ok = wait(FQ ? bars.q_ready[qb] : bars.q_full[qb], (item_cnt / C::QBUF) & 1))) break;
                 // prologue: S of the item's first key tile
                 if (!(ok = wait(bars.k_full[st], ph))) break;
                 if (t > 0 && !(ok = wait(b_sfree, (t - 1) & 1))) break;
@@ -292,6 +316,37 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // drain: nothing this thread issued may still be running when TMEM is freed
             mma_commit(bar_addr(bars.drain[ti]));
             mbar_wait(bar_addr(bars.drain[ti]), 0, (const volatile int *)&s_abort, ok ? kWaitBudget : 200000000ll);
+        }
+    } else if (warp == 3) {
+        if constexpr (FQ) {
+            // -------------------------------------------------------- raw Q -> normalised, rotated Q
+            // Lane l takes rows l, l + 32, .. of the item's 256; each row is read and rewritten in
+            // place through its 32-byte-swizzled slabs (16-byte chunk index XOR bit 2 of the row,
+            // the layout the TMA wrote and the MMA descriptors read). Rows past the segment end
+            // belong to no result and are left as loaded.
+            uint32_t item_cnt = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_cnt) {
+                const Item item = items[it];
+                const int64_t seg_end = (int64_t)item.x + item.y, q0 = item.z;
+                const uint32_t qb = item_cnt % C::QBUF;
+                if (!(ok = wait_warp(bars.q_full[qb], (item_cnt / C::QBUF) & 1))) break;
+                unsigned char *qbuf = base + C::OFF_Q + 2 * qb * C::Q_TILE;
+#pragma unroll 1
+                for (int k = 0; k < 2 * BM / 32; ++k) {
+                    const int row = lane + 32 * k;
+                    if (q0 + row >= seg_end) continue;
+                    const int r = row % BM;
+                    unsigned char *tile = qbuf + (row / BM) * C::Q_TILE + 32 * r;
+                    const int sw = ((r >> 2) & 1) << 4;
+                    rope::transform_row<D>(qr, q0 + row, [&](int c) {
+                        return reinterpret_cast<uint4 *>(tile + (c >> 1) * C::Q_SLAB + (((c & 1) << 4) ^ sw));
+                    });
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_addr(bars.q_ready[qb]));
+            }
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax groups
@@ -476,7 +531,8 @@ cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, int stal
         !make_map(&mv, a.v, a.T, a.H, D, a.v_stride, C::BN))
         return cudaErrorInvalidValue;
     // the lse store is compiled in only where it is asked for: the plain kernel keeps its code unchanged
-    auto kern = a.lse ? attn_long_kernel<D, true> : attn_long_kernel<D, false>;
+    auto kern = a.lse ? (a.fuse_q ? attn_long_kernel<D, true, true> : attn_long_kernel<D, true, false>)
+                      : (a.fuse_q ? attn_long_kernel<D, false, true> : attn_long_kernel<D, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     // the setmaxnreg split assumes exactly this launch budget; refuse anything else rather than wait on it
@@ -489,7 +545,7 @@ cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, int stal
     LaunchScope scope("attn_long", stream);
     kern<<<blocks, kThreads, C::SMEM, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16 *>(a.out),
                                                                a.out_stride, a.lse, a.H, a.scale_log2, a.hdr,
-                                                               a.items, a.status, stall_v);
+                                                               a.items, a.status, stall_v, a.qr);
     return cudaGetLastError();
 }
 

@@ -51,6 +51,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool v
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;\n" ::); }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -94,12 +95,13 @@ __device__ __forceinline__ void load_rows(__nv_bfloat16 *s, const __nv_bfloat16 
     }
 }
 
-template <int D>
+template <int D, bool FQ>
 __global__ void __launch_bounds__(kThreads, ShortCfg<D>::MIN_BLOCKS)
 attn_short_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                   const __nv_bfloat16 *__restrict__ v, int64_t q_stride, int64_t k_stride, int64_t v_stride,
                   __nv_bfloat16 *__restrict__ out, int64_t out_stride, float *__restrict__ lse, int H,
-                  float scale_log2, const WsHeader *__restrict__ hdr, const Item *__restrict__ items)
+                  float scale_log2, const WsHeader *__restrict__ hdr, const Item *__restrict__ items,
+                  const rope::QRope qr)
 {
     using C = ShortCfg<D>;
     constexpr int PITCH = C::PITCH;
@@ -127,6 +129,7 @@ attn_short_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
 
         __syncthreads();                                     // smem of the previous item is free
         load_rows<D>(sQ, qh, q_stride, q0, (q_valid + 15) & ~15, q_valid);
+        if constexpr (FQ) cp_async_commit();                // Q in a group of its own
 
         float o[2][DN][4];
 #pragma unroll
@@ -143,6 +146,20 @@ attn_short_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
             load_rows<D>(sK, kh, k_stride, kv0, (kv_valid + 15) & ~15, kv_valid);
             load_rows<D>(sV, vh, v_stride, kv0, (kv_valid + 15) & ~15, kv_valid);
             cp_async_commit();
+            if constexpr (FQ) {
+                // raw Q: once its group has landed, thread r normalises and rotates row r in shared
+                // memory (the prologue kernel's arithmetic, in the same order) while the first K/V
+                // tile is still on its way
+                if (j == 0) {
+                    cp_async_wait_one();
+                    __syncthreads();
+                    const int r = threadIdx.x;
+                    if (r < q_valid)
+                        rope::transform_row<D>(qr, (int64_t)q0 + r, [&](int c) {
+                            return reinterpret_cast<uint4 *>(sQ + r * PITCH + 8 * c);
+                        });
+                }
+            }
             cp_async_wait_all();
             __syncthreads();
             if (!act0) continue;                             // warp-uniform: nothing of the segment in its rows
@@ -294,19 +311,20 @@ cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, cudaStre
 {
     constexpr size_t smem = ShortCfg<D>::SMEM;
     static_assert(smem <= 227 * 1024, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(attn_short_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = a.fuse_q ? attn_short_kernel<D, true> : attn_short_kernel<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_short_kernel<D>, kThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
     if (e != cudaSuccess) return e;
     const int64_t cap = (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
     const unsigned blocks = (unsigned)(max_items < cap ? max_items : cap);
     if (blocks == 0) return cudaSuccess;
     LaunchScope scope("attn_short", stream);
-    attn_short_kernel<D><<<blocks, kThreads, smem, stream>>>(
+    kern<<<blocks, kThreads, smem, stream>>>(
         static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k),
         static_cast<const __nv_bfloat16 *>(a.v), a.q_stride, a.k_stride, a.v_stride,
-        static_cast<__nv_bfloat16 *>(a.out), a.out_stride, a.lse, a.H, a.scale_log2, a.hdr, a.items);
+        static_cast<__nv_bfloat16 *>(a.out), a.out_stride, a.lse, a.H, a.scale_log2, a.hdr, a.items, a.qr);
     return cudaGetLastError();
 }
 

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "vit_attn.h"
+#include "rope_math.cuh"
 
 namespace vit {
 
@@ -56,6 +57,9 @@ cudaError_t launch_rope_freqs(int dim, float theta, const int32_t *grid_hw, int 
                               float *inv_freq, int32_t *pos_hw, int32_t *cu_seqlens, int32_t *status,
                               cudaStream_t stream);
 
+cudaError_t launch_rope_table(const float *inv_freq, int n_freq, int max_pos, float *cos_sin,
+                              cudaStream_t stream);
+
 // q_in/q_out or k_in/k_out may both be NULL (that half is skipped); interleaved selects adjacent pairs.
 cudaError_t launch_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T,
                                 int H, int D, int64_t q_in_stride, int64_t q_out_stride,
@@ -79,6 +83,8 @@ struct AttnArgs {
     const WsHeader *hdr;
     const Item *items;
     int32_t *status;
+    bool fuse_q;                // q holds raw values: normalise and rotate each Q tile after it is loaded
+    rope::QRope qr;             // how (when fuse_q)
 };
 
 cudaError_t launch_attn_short(const AttnArgs &a, int64_t max_items_short, int num_sms, cudaStream_t stream);

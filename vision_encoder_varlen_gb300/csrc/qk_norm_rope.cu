@@ -23,64 +23,18 @@
 // inside each of its two chunks. Either q or k may be left out (its pointers
 // NULL), which turns the pass into a one-tensor pre-stage.
 #include "internal.h"
+#include "rope_math.cuh"
 
 namespace vit {
 namespace {
+
+using namespace rope;
 
 constexpr int kThreads = 256;
 constexpr int kTokensPerIter = 8;
 constexpr int kRowBatch = 4;                           // rows per group whose loads are in flight together
 constexpr int kGroup = 8;                              // lanes per row
 constexpr int kGroupsPerBlock = kThreads / kGroup;     // 32
-
-__device__ __forceinline__ void unpack8(const uint4 &u, float *f) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// ---- packed pairs: Blackwell f32x2 arithmetic and bf16x2 multiply
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-    uint64_t v;
-    asm("mov.b64 %0, {%1, %2};\n" : "=l"(v) : "f"(lo), "f"(hi));
-    return v;
-}
-__device__ __forceinline__ void f2_split(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-// bf16(bf16(x0*inv) * w0), bf16(bf16(x1*inv) * w1) as two floats: the product of two bf16
-// values is exact in fp32, so one bf16x2 multiply rounds exactly like the scalar form
-__device__ __forceinline__ void norm_pair(float &x0, float &x1, float inv, uint32_t w2) {
-    const uint32_t t = pack2(x0 * inv, x1 * inv);
-    __nv_bfloat162 y = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&t),
-                               *reinterpret_cast<const __nv_bfloat162 *>(&w2));
-    const uint32_t u = *reinterpret_cast<uint32_t *>(&y);
-    x0 = __uint_as_float(u << 16);
-    x1 = __uint_as_float(u & 0xffff0000u);
-}
 
 template <int D, bool IL>
 __global__ void __launch_bounds__(kThreads)
@@ -156,60 +110,29 @@ qk_norm_rope_kernel(const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out,
                 unpack8(va[k], xa);
                 unpack8(vb[k], xb);
                 if (use_norm) {
-                    float ss = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) ss = fmaf(xa[i], xa[i], fmaf(xb[i], xb[i], ss));
+                    // per-lane chunk sums combined by the xor tree of combine8 (idle lanes add 0)
+                    float ss = chunk_sumsq(xa, xb);
                     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
                     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
                     ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-                    const float inv = rsqrtf(ss / (float)D + eps);
+                    const float inv = inv_rms(ss, D, eps);
                     if (act[k]) {                                // idle lanes (c >= CHUNKS) read nothing
-                        const uint4 wa = *reinterpret_cast<const uint4 *>(&s_w[which_[k]][c * 4]);
-                        const uint4 wb = *reinterpret_cast<const uint4 *>(&s_w[which_[k]][HALF / 2 + c * 4]);
-                        const uint32_t wa_[4] = {wa.x, wa.y, wa.z, wa.w}, wb_[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-                        for (int i = 0; i < 8; i += 2) {
-                            norm_pair(xa[i], xa[i + 1], inv, wa_[i / 2]);
-                            norm_pair(xb[i], xb[i + 1], inv, wb_[i / 2]);
-                        }
+                        norm8(xa, inv, *reinterpret_cast<const uint4 *>(&s_w[which_[k]][c * 4]));
+                        norm8(xb, inv, *reinterpret_cast<const uint4 *>(&s_w[which_[k]][HALF / 2 + c * 4]));
                     }
                 }
                 if (act[k]) {
-                    uint32_t oa[4], ob[4];
+                    uint4 oa, ob;
                     if constexpr (!IL) {
-                        const float4 *cs_ = s_cs[tt_[k]] + c * 4;
-#pragma unroll
-                        for (int i = 0; i < 8; i += 2) {
-                            const float4 t = cs_[i / 2];
-                            const uint64_t cc = f2(t.x, t.y), sn = f2(t.z, t.w);
-                            const uint64_t a = f2(xa[i], xa[i + 1]), b = f2(xb[i], xb[i + 1]);
-                            float ya0, ya1, yb0, yb1;
-                            f2_split(f2_sub(f2_mul(a, cc), f2_mul(b, sn)), ya0, ya1);     // x cos - x' sin
-                            f2_split(f2_fma(a, sn, f2_mul(b, cc)), yb0, yb1);             // x' cos + x sin
-                            oa[i / 2] = pack2(ya0, ya1);
-                            ob[i / 2] = pack2(yb0, yb1);
-                        }
+                        rotate_half8(xa, xb, s_cs[tt_[k]] + c * 4, oa, ob);
                     } else {
                         // chunk c of the first half holds pairs 4c..4c+3, the second half's chunk c
                         // pairs D/4 + 4c .. D/4 + 4c + 3 (D/4 is even, so both start a float4 entry)
-                        const float4 *csa = s_cs[tt_[k]] + 2 * c, *csb = s_cs[tt_[k]] + D / 8 + 2 * c;
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            const float4 ta = csa[p >> 1], tb = csb[p >> 1];
-                            const float ca = (p & 1) ? ta.y : ta.x, sa = (p & 1) ? ta.w : ta.z;
-                            const float cb = (p & 1) ? tb.y : tb.x, sb = (p & 1) ? tb.w : tb.z;
-                            float y0, y1;
-                            // (x0 cos - x1 sin, x1 cos + x0 sin) = (x0, x1) * cos + (x1, x0) * (-sin, sin)
-                            f2_split(f2_fma(f2(xa[2 * p + 1], xa[2 * p]), f2(-sa, sa),
-                                            f2_mul(f2(xa[2 * p], xa[2 * p + 1]), f2(ca, ca))), y0, y1);
-                            oa[p] = pack2(y0, y1);
-                            f2_split(f2_fma(f2(xb[2 * p + 1], xb[2 * p]), f2(-sb, sb),
-                                            f2_mul(f2(xb[2 * p], xb[2 * p + 1]), f2(cb, cb))), y0, y1);
-                            ob[p] = pack2(y0, y1);
-                        }
+                        oa = interleaved8(xa, s_cs[tt_[k]] + 2 * c);
+                        ob = interleaved8(xb, s_cs[tt_[k]] + D / 8 + 2 * c);
                     }
-                    *reinterpret_cast<uint4 *>(dst[k]) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-                    *reinterpret_cast<uint4 *>(dst[k] + HALF) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+                    *reinterpret_cast<uint4 *>(dst[k]) = oa;
+                    *reinterpret_cast<uint4 *>(dst[k] + HALF) = ob;
                 }
             }
         }

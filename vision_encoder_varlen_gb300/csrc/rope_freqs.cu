@@ -83,7 +83,37 @@ rope_freqs_kernel(int dim, float theta, const int32_t *__restrict__ grid_hw, int
     }
 }
 
+// cos/sin of p * inv_freq[f] for every position p < max_pos and frequency f < n_freq
+// (VisionRotaryEmbedding's table over positions, indexed later by each token's row and
+// column): entry (p, f/2) = {cos a_f, cos a_f+1, sin a_f, sin a_f+1}, the same fp32
+// product and sincosf the prologue kernel evaluates per token.
+__global__ void __launch_bounds__(kThreads)
+rope_table_kernel(const float *__restrict__ inv_freq, int n_freq, int max_pos, float4 *__restrict__ cs)
+{
+    const int per = n_freq / 2;
+    const int64_t n = (int64_t)max_pos * per;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads) {
+        const int p = (int)(i / per), f = 2 * (int)(i % per);
+        const float pos = (float)p;
+        float s0, c0, s1, c1;
+        sincosf(pos * inv_freq[f], &s0, &c0);
+        sincosf(pos * inv_freq[f + 1], &s1, &c1);
+        cs[i] = make_float4(c0, c1, s0, s1);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_rope_table(const float *inv_freq, int n_freq, int max_pos, float *cos_sin, cudaStream_t stream)
+{
+    const int64_t n = (int64_t)max_pos * (n_freq / 2);
+    if (n == 0) return cudaSuccess;
+    const int64_t want = (n + kThreads - 1) / kThreads;
+    const unsigned blocks = (unsigned)(want < 4096 ? want : 4096);
+    LaunchScope scope("rope_table", stream);
+    rope_table_kernel<<<blocks, kThreads, 0, stream>>>(inv_freq, n_freq, max_pos, reinterpret_cast<float4 *>(cos_sin));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_rope_freqs(int dim, float theta, const int32_t *grid_hw, int n_img, int64_t T,
                               float *inv_freq, int32_t *pos_hw, int32_t *cu_seqlens, int32_t *status,

@@ -26,6 +26,11 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
+// shared-memory writes of ordinary stores become visible to the async proxy (TMA, tcgen05.mma)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
