@@ -282,6 +282,39 @@ vit_status_t vit_varlen_attn_fused_q(const void *q, const void *k, const void *v
                                      void *workspace, size_t workspace_bytes,
                                      int32_t *status_dev, vit_stream_t stream);
 
+/*
+ * Attention over a padded layout: segment i is the rows [seq_start[i],
+ * seq_start[i] + seq_len[i]) of q, k, v and out, and the rows between
+ * segments are padding that is neither read nor written.
+ *
+ * [TS] vision_attn_flashinfer_cudnn takes per-sequence element offsets for
+ * q/k, v and o plus the real (un-padded) sequence_lengths, with max_seqlen as
+ * the bucketed budget, so a CUDA graph captured for one bucket of sizes can be
+ * replayed for any batch that fits it. Here the offsets are token rows shared
+ * by all four tensors (each tensor keeps its own token stride, which is what
+ * the page's per-tensor element offsets encode for packed qkv), and nothing
+ * on the host depends on the lengths: capture once with the bucket's T, B and
+ * max_seqlen, then replay after writing new starts and lengths on the device.
+ *
+ * Arguments as for vit_varlen_attn_lse, except:
+ *   seq_start   device int32 [B]: first row of each segment, ascending.
+ *   seq_len     device int32 [B]: real length of each segment (0 allowed).
+ *               Checked on the device: every segment inside [0, T), after the
+ *               previous segment's end, and no longer than max_seqlen;
+ *               otherwise VIT_ERR_BAD_SEQLENS / VIT_ERR_SEQLEN_EXCEEDS_MAX and
+ *               nothing is computed.
+ *   B           0 <= B <= VIT_MAX_SEGMENTS (0: nothing to do).
+ *   q_rope      NULL, or the fused Q normalisation of vit_varlen_attn_fused_q.
+ * The workspace size is vit_varlen_attn_workspace_size(T, H, B, D).
+ */
+vit_status_t vit_varlen_attn_padded(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                    int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                                    const int32_t *seq_start, const int32_t *seq_len, int B,
+                                    int max_seqlen, float scale, void *out, int64_t out_stride,
+                                    float *lse, const vit_q_rope_t *q_rope,
+                                    void *workspace, size_t workspace_bytes,
+                                    int32_t *status_dev, vit_stream_t stream);
+
 /* Size of the fixed device scratch array behind vit_varlen_attn_noalloc (per GPU). */
 #define VIT_NOALLOC_WORKSPACE_BYTES (4u << 20)
 

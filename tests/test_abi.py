@@ -149,6 +149,20 @@ def test_fused_q_and_table_validation_without_gpu(L):
     assert fused(QR(16, 16, 64, 18, 1e-6, 0)) == -5             # weight not 16-byte aligned
 
 
+def test_padded_call_validation_without_gpu(L):
+    p = ctypes.c_void_p
+
+    def padded(B, start, length, D=80):
+        return L.vit_varlen_attn_padded(p(16), p(16), p(16), 4096, 2, D, 160, 160, 160,
+                                        None if start is None else p(start), None if length is None else p(length),
+                                        B, 512, 0.0, p(16), 160, None, None, p(256), 1 << 20, None, None)
+    assert padded(0, None, None) == 0              # nothing to compute
+    assert padded(2, 16, None) == -1
+    assert padded(2, None, 16) == -1
+    assert padded(2, 16, 18) == -5                 # seq_len not 4-byte aligned
+    assert padded(2, 16, 16, D=81) == -2
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import importlib
     monkeypatch.setattr(vit, "_lib", None)

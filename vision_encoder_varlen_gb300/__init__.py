@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
             L.vit_varlen_attn_fused_q.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, ctypes.POINTER(_QRope),
                                                   vp, i32, i32, f32, vp, i64, vp, vp, sz, vp, vp]
             L.vit_rope_table.argtypes = [vp, i32, i32, vp, vp]
+            L.vit_varlen_attn_padded.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, vp, vp, i32, i32, f32, vp,
+                                                 i64, vp, ctypes.POINTER(_QRope), vp, sz, vp, vp]
             L.vit_read_status.argtypes = [vp, vp]
             L.vit_set_short_segment_max.argtypes = [i32]
             L.vit_set_short_segment_max.restype = i32
@@ -79,6 +81,7 @@ def lib() -> ctypes.CDLL:
             L.vit_kernel_timing_read.argtypes = [ctypes.POINTER(_KernelTime), i32]
             for fn in ("vit_device_supported", "vit_rope_freqs", "vit_qk_norm_rope", "vit_qk_norm_rope_ex",
                        "vit_varlen_attn", "vit_varlen_attn_lse", "vit_varlen_attn_fused_q", "vit_rope_table",
+                       "vit_varlen_attn_padded",
                        "vit_read_status", "vit_kernel_timing", "vit_kernel_timing_read"):
                 getattr(L, fn).restype = i32
             _lib = L
@@ -283,6 +286,37 @@ def varlen_attn_fused_q(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_se
                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
                                          _ptr(status), _stream(stream)), "vit_varlen_attn_fused_q")
     return (out, lse) if lse is not None else out
+
+
+def varlen_attn_padded(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_start: torch.Tensor,
+                       seq_len: torch.Tensor, max_seqlen: int, scale: float | None = None, *,
+                       out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                       status: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """Attention over a padded layout: segment i is rows [seq_start[i], seq_start[i] + seq_len[i]) of
+    q, k, v and out (ascending, not overlapping); rows between segments are left untouched. Nothing
+    on the host depends on the lengths, so the call can be captured in a CUDA graph and replayed
+    after new starts/lengths are written into the same device tensors."""
+    T, H, D = q.shape
+    qs, ks, vs = _tok_stride(q, "q", H, D), _tok_stride(k, "k", H, D), _tok_stride(v, "v", H, D)
+    for name, t in (("seq_start", seq_start), ("seq_len", seq_len)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA int32 tensor [B]")
+    B = seq_len.numel()
+    if seq_start.numel() != B:
+        raise ValueError("seq_start and seq_len must have the same length")
+    if out is None:
+        out = torch.empty((T, H, D), dtype=q.dtype, device=q.device)
+    os_ = _tok_stride(out, "out", H, D)
+    if workspace is None:
+        workspace = torch.empty(max(workspace_size(T, H, B, D), 16), dtype=torch.uint8, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (T, H) or not lse.is_contiguous()):
+        raise ValueError(f"lse must be a contiguous CUDA float32 tensor [{T}, {H}]")
+    _check(lib().vit_varlen_attn_padded(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, _ptr(seq_start),
+                                        _ptr(seq_len), B, int(max_seqlen), float(scale) if scale is not None else 0.0,
+                                        _ptr(out), os_, _ptr(lse), None, _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
+           "vit_varlen_attn_padded")
+    return out
 
 
 def encoder_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen: int,

@@ -181,17 +181,23 @@ namespace {
 
 vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64_t T, int H, int D, int64_t q_stride,
                               int64_t k_stride, int64_t v_stride, const vit_q_rope_t *q_rope,
-                              const int32_t *cu_seqlens, int B, int max_seqlen, float scale, void *out,
-                              int64_t out_stride, float *lse, void *workspace, size_t workspace_bytes,
-                              int32_t *status_dev, vit_stream_t stream)
+                              const int32_t *cu_seqlens, const int32_t *seq_start, const int32_t *seq_len, int B,
+                              int max_seqlen, float scale, void *out, int64_t out_stride, float *lse,
+                              void *workspace, size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
 {
+    const bool padded = seq_len != nullptr;
     if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
     if (T < 0 || T >= kMaxTokens || H < 1 || B < 0) return VIT_ERR_BAD_SHAPE;
     if (B > VIT_MAX_SEGMENTS) return VIT_ERR_TOO_MANY_SEGMENTS;
     if (B == 0) return T == 0 ? VIT_OK : VIT_ERR_BAD_SHAPE;
     if (max_seqlen < 0 || (T > 0 && max_seqlen < 1)) return VIT_ERR_BAD_ARGUMENT;
     if (isnan(scale) || isinf(scale)) return VIT_ERR_BAD_ARGUMENT;
-    if (!cu_seqlens && T % B != 0) return VIT_ERR_BAD_ARGUMENT;
+    if (padded) {
+        if (!seq_start) return VIT_ERR_NULL_POINTER;
+        if (((uintptr_t)seq_start & 3u) || ((uintptr_t)seq_len & 3u)) return VIT_ERR_MISALIGNED;
+    } else if (!cu_seqlens && T % B != 0) {
+        return VIT_ERR_BAD_ARGUMENT;
+    }
     if (T > 0) {
         if (!q || !k || !v || !out) return VIT_ERR_NULL_POINTER;
         if (!stride_ok(q_stride, H, D) || !stride_ok(k_stride, H, D) || !stride_ok(v_stride, H, D) ||
@@ -227,7 +233,8 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
     sp.short_max = g_short_max.load();
     sp.bm_long = attn_long_bm();
     sp.bm_short = attn_short_bm();
-    cudaError_t e = launch_schedule(cu_seqlens, B, T, H, max_seqlen, sp, hdr, items, status_dev, s);
+    cudaError_t e = launch_schedule(padded ? nullptr : cu_seqlens, seq_start, seq_len, B, T, H, max_seqlen, sp, hdr,
+                                    items, status_dev, s);
     if (e != cudaSuccess) return VIT_ERR_CUDA;
     if (T == 0) return VIT_OK;
     AttnArgs a;
@@ -259,7 +266,7 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
         a.qr.status = status_dev;
     }
     // a segment can only be long when the bound allows it
-    const int64_t longest = cu_seqlens ? (int64_t)max_seqlen : T / B;
+    const int64_t longest = (cu_seqlens || padded) ? (int64_t)max_seqlen : T / B;
     if (longest > sp.short_max) {
         e = launch_attn_long(a, max_items(T, H, B, sp.bm_long), sms, g_stall_v.load(), s);
         if (e != cudaSuccess) return VIT_ERR_CUDA;
@@ -277,8 +284,8 @@ vit_status_t vit_varlen_attn_lse(const void *q, const void *k, const void *v, in
                                  int B, int max_seqlen, float scale, void *out, int64_t out_stride, float *lse,
                                  void *workspace, size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
 {
-    return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, nullptr, cu_seqlens, B, max_seqlen,
-                            scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
+    return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, nullptr, cu_seqlens, nullptr, nullptr, B,
+                            max_seqlen, scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
 }
 
 vit_status_t vit_varlen_attn_fused_q(const void *q, const void *k, const void *v, int64_t T, int H, int D,
@@ -288,8 +295,22 @@ vit_status_t vit_varlen_attn_fused_q(const void *q, const void *k, const void *v
                                      size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
 {
     if (!q_rope) return VIT_ERR_NULL_POINTER;
-    return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, q_rope, cu_seqlens, B, max_seqlen,
-                            scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
+    return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, q_rope, cu_seqlens, nullptr, nullptr, B,
+                            max_seqlen, scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
+}
+
+vit_status_t vit_varlen_attn_padded(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                    int64_t q_stride, int64_t k_stride, int64_t v_stride, const int32_t *seq_start,
+                                    const int32_t *seq_len, int B, int max_seqlen, float scale, void *out,
+                                    int64_t out_stride, float *lse, const vit_q_rope_t *q_rope, void *workspace,
+                                    size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
+{
+    if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
+    if (T < 0 || T >= kMaxTokens || H < 1 || B < 0) return VIT_ERR_BAD_SHAPE;
+    if (B == 0) return VIT_OK;                           // every row is padding: nothing to compute
+    if (!seq_len || !seq_start) return VIT_ERR_NULL_POINTER;
+    return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, q_rope, nullptr, seq_start, seq_len, B,
+                            max_seqlen, scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
 }
 
 vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_t T, int H, int D, int64_t q_stride,

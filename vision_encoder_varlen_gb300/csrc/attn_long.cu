@@ -38,6 +38,8 @@
 // VIT_ERR_TIMEOUT, and all roles drain and free TMEM before exiting.
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "sm100.cuh"
 
@@ -90,6 +92,33 @@ struct Bars {
 };
 
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_addr(&b); }
+
+// P.V of the last tile of a segment that ends inside the tile: only the 16-key steps that hold a
+// key of the segment, with the rows of the last step past the segment's end zeroed first. Those
+// rows get P = 0, but 0 * (Inf or NaN) is NaN, so without this a non-finite value in the next
+// segment or in padding would reach this segment's output. V has landed (v_full) when this runs,
+// and both issuers write the same zeros, so their order does not matter. Called only from the copy
+// of the issuer's tile step that follows its loop over full tiles (inlined there: measured as fast
+// as before on the full tiles, where an out-of-line call was 0.5 % slower).
+template <int NSLAB, int SLAB, int D>
+__device__ __forceinline__ void pv_tail(uint32_t tO, uint32_t tP, uint64_t dv, unsigned char *vt, uint32_t acc,
+                                     int kv_valid, uint32_t bar_done)
+{
+    constexpr uint32_t ID_PV = idesc_bf16(128, D, 0, 1);
+    const int n16 = (kv_valid + 15) >> 4;
+    if (kv_valid & 15) {
+        for (int r = kv_valid; r < 16 * n16; ++r)
+            for (int s = 0; s < NSLAB; ++s) {
+                uint4 *p = reinterpret_cast<uint4 *>(vt + s * SLAB + 32 * r);
+                p[0] = make_uint4(0u, 0u, 0u, 0u);
+                p[1] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        fence_proxy_async_smem();
+    }
+    for (int kk = 0; kk < n16; ++kk)
+        mma_ts(tO, tP + kk * 8, dv + (uint64_t)(kk * (512 >> 4)), ID_PV, kk > 0 ? 1u : acc);
+    mma_commit(bar_done);
+}
 
 template <int D, bool LSE, bool FQ>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -281,6 +310,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_cnt) {
                 const Item item = items[it];
                 const int n_kv = (item.y + BN - 1) / BN;
+                const int n_full = item.y / BN;                  // tiles with BN keys of the segment
                 uint32_t st = t % ST, ph = (t / ST) & 1;
                 const uint32_t qb = item_cnt % C::QBUF;         // Q buffer of this item
                 const uint64_t dq = dq_base + qb * ((2 * C::Q_TILE) >> 4);
@@ -291,26 +321,37 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_after();
                 qk(dq, dk0 + st * STAGE_STEP);
                 if (n_kv == 1) mma_commit(bar_addr(bars.q_empty[qb]));
-                for (int j = 0; j < n_kv; ++j) {
+                // one key tile: QK of the next tile, then P.V of this one; the tail variant (the last
+                // tile of a segment that ends inside it) is a separate copy after the loop, so the
+                // loop over full tiles carries no test for it
+                auto step = [&](int j, auto tail) -> bool {
                     const uint32_t u = t + j;                 // global index of this key tile
                     const uint32_t st1 = (st + 1 == (uint32_t)ST) ? 0u : st + 1;
                     const uint32_t ph1 = (st + 1 == (uint32_t)ST) ? ph ^ 1u : ph;
                     if (j + 1 < n_kv) {                        // next tile's S as soon as this S was read
-                        if (!(ok = wait(bars.k_full[st1], ph1))) break;
-                        if (!(ok = wait(b_sfree, u & 1))) break;
+                        if (!(ok = wait(bars.k_full[st1], ph1))) return false;
+                        if (!(ok = wait(b_sfree, u & 1))) return false;
                         tc_fence_after();
                         qk(dq, dk0 + st1 * STAGE_STEP);
                         if (j + 2 == n_kv) mma_commit(bar_addr(bars.q_empty[qb]));
                     }
-                    if (!(ok = wait(bars.v_full[st], ph))) break;
-                    if (j == 0 && item_cnt > 0 && !(ok = wait(b_ofree, (item_cnt - 1) & 1))) break;
-                    if (!(ok = wait(b_pfull, u & 1))) break;
+                    if (!(ok = wait(bars.v_full[st], ph))) return false;
+                    if (j == 0 && item_cnt > 0 && !(ok = wait(b_ofree, (item_cnt - 1) & 1))) return false;
+                    if (!(ok = wait(b_pfull, u & 1))) return false;
                     tc_fence_after();
-                    pv(dv0 + st * STAGE_STEP, j > 0 ? 1u : 0u);
+                    if constexpr (decltype(tail)::value)
+                        pv_tail<NSLAB, C::KV_SLAB, D>(tO, tP, dv0 + st * STAGE_STEP, base + C::OFF_V + st * C::KV_TILE,
+                                                      j > 0 ? 1u : 0u, item.y - j * BN, a_pvdone);
+                    else
+                        pv(dv0 + st * STAGE_STEP, j > 0 ? 1u : 0u);
                     mma_commit(bar_addr(bars.kv_empty[st]));
                     st = st1;
                     ph = ph1;
-                }
+                    return true;
+                };
+                for (int j = 0; j < n_full; ++j)
+                    if (!step(j, std::false_type{})) break;
+                if (ok && n_full < n_kv) step(n_full, std::true_type{});
                 t += n_kv;
             }
             // drain: nothing this thread issued may still be running when TMEM is freed
@@ -533,13 +574,18 @@ cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, int stal
     // the lse store is compiled in only where it is asked for: the plain kernel keeps its code unchanged
     auto kern = a.lse ? (a.fuse_q ? attn_long_kernel<D, true, true> : attn_long_kernel<D, true, false>)
                       : (a.fuse_q ? attn_long_kernel<D, false, true> : attn_long_kernel<D, false, false>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    static DeviceOnce once[4];                           // per (lse, fused Q) variant
+    cudaError_t e = once[(a.lse ? 2 : 0) + (a.fuse_q ? 1 : 0)].run([&] {
+        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (r != cudaSuccess) return r;
+        // the setmaxnreg split assumes exactly this launch budget; refuse anything else rather than wait on it
+        cudaFuncAttributes fa;
+        r = cudaFuncGetAttributes(&fa, kern);
+        if (r != cudaSuccess) return r;
+        return (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) ? cudaErrorInvalidConfiguration
+                                                                              : cudaSuccess;
+    });
     if (e != cudaSuccess) return e;
-    // the setmaxnreg split assumes exactly this launch budget; refuse anything else rather than wait on it
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
     const unsigned blocks = (unsigned)(max_items < num_sms ? max_items : num_sms);
     if (blocks == 0) return cudaSuccess;
     LaunchScope scope("attn_long", stream);

@@ -312,11 +312,20 @@ cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, cudaStre
     constexpr size_t smem = ShortCfg<D>::SMEM;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     auto kern = a.fuse_q ? attn_short_kernel<D, true> : attn_short_kernel<D, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static DeviceOnce once[2];                           // per fused-Q variant
+    static int per_sm_of[2][64];                         // resident CTAs per SM, per variant and device
+    const int var = a.fuse_q ? 1 : 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    e = once[var].run([&] {
+        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (r != cudaSuccess) return r;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_of[var][dev], kern, kThreads, smem);
+    });
     if (e != cudaSuccess) return e;
+    const int per_sm = per_sm_of[var][dev];
     const int64_t cap = (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
     const unsigned blocks = (unsigned)(max_items < cap ? max_items : cap);
     if (blocks == 0) return cudaSuccess;

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "vit_attn.h"
 #include "rope_math.cuh"
 
@@ -43,6 +45,23 @@ __device__ __forceinline__ void report_error(int32_t *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// One-time setup per device of a kernel's launch attributes (dynamic shared memory limit,
+// register checks, occupancy). Done on the first launch on each device, so later calls,
+// including ones made while a stream is being captured into a CUDA graph, only launch.
+struct DeviceOnce {
+    std::atomic<uint64_t> done{0};
+    template <typename F> cudaError_t run(F &&fn) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+        if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+        e = fn();
+        if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+        return e;
+    }
+};
+
 // ---- launch bookkeeping (instrument.cpp) ----
 struct LaunchScope {
     LaunchScope(const char *name, cudaStream_t stream);
@@ -67,9 +86,11 @@ cudaError_t launch_qk_norm_rope(const void *q_in, void *q_out, const void *k_in,
                                 const float *inv_freq, const void *norm_w, float eps, bool interleaved,
                                 int num_sms, cudaStream_t stream);
 
-cudaError_t launch_schedule(const int32_t *cu_seqlens, int B, int64_t T, int H, int max_seqlen,
-                            SchedParams sp, WsHeader *hdr, Item *items, int32_t *status,
-                            cudaStream_t stream);
+// segments from cu_seqlens (contiguous; NULL = B uniform segments) or, when seq_len is
+// given, from per-segment starts and lengths (a padded layout)
+cudaError_t launch_schedule(const int32_t *cu_seqlens, const int32_t *seq_start, const int32_t *seq_len, int B,
+                            int64_t T, int H, int max_seqlen, SchedParams sp, WsHeader *hdr, Item *items,
+                            int32_t *status, cudaStream_t stream);
 
 // Everything both attention kernels read, validated by the API layer.
 struct AttnArgs {

@@ -121,11 +121,12 @@ cudaError_t launch_rope_freqs(int dim, float theta, const int32_t *grid_hw, int 
 {
     const int64_t blocks = T > 0 ? (T + kTokensPerBlock - 1) / kTokensPerBlock : 1;
     const size_t smem = sizeof(int64_t) * (size_t)(n_img + 1);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(rope_freqs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    static DeviceOnce once;                              // the limit for the largest grid list, set once
+    cudaError_t e = once.run([] {
+        return cudaFuncSetAttribute(rope_freqs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(sizeof(int64_t) * (VIT_MAX_SEGMENTS + 1)));
+    });
+    if (e != cudaSuccess) return e;
     LaunchScope scope("rope_freqs", stream);
     rope_freqs_kernel<<<(unsigned)blocks, kThreads, smem, stream>>>(
         dim, theta, grid_hw, n_img, T, inv_freq, reinterpret_cast<int2 *>(pos_hw), cu_seqlens, status);

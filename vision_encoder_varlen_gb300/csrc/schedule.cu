@@ -5,7 +5,11 @@
 // keeps max_seqlen off the GPU->CPU path for the same reason), one block:
 //   1. validates the offsets (cu[0] == 0, non-decreasing, cu[B] == T, every
 //      length <= max_seqlen; max_seqlen may be a padded bucket bound,
-//      round_up_to_bucket on the same page);
+//      round_up_to_bucket on the same page). A padded layout (per-segment
+//      start and real length, as the cuDNN path's offsets and
+//      sequence_lengths describe) is taken instead when seq_len is given:
+//      starts ascending, segments inside [0, T) and not overlapping; the rows
+//      between them are padding that nothing reads or writes;
 //   2. orders segments longest first (LPT) with a bitonic sort of
 //      (length desc, index asc) keys, so the order is deterministic;
 //   3. expands every segment into (segment, head, q-block) work items: long
@@ -50,7 +54,8 @@ __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t *s_wa
 }
 
 __global__ void __launch_bounds__(kThreads)
-schedule_kernel(const int32_t *__restrict__ cu_seqlens, int B, int64_t T, int H, int max_seqlen,
+schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restrict__ seq_start,
+                const int32_t *__restrict__ seq_len, int B, int64_t T, int H, int max_seqlen,
                 SchedParams sp, WsHeader *hdr, Item *items, int32_t *status)
 {
     extern __shared__ unsigned long long s_key[];      // [NP] sort keys, then [B] int32 offsets reuse
@@ -70,15 +75,23 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, int B, int64_t T, int H,
     const int64_t uni = B > 0 ? T / B : 0;
     for (int i = tid; i < B; i += kThreads) {
         int64_t a, b;
-        if (cu_seqlens) {
-            a = cu_seqlens[i];
-            b = cu_seqlens[i + 1];
+        if (seq_len) {
+            a = seq_start[i];
+            b = a + seq_len[i];
+            // inside [0, T), after the previous segment's end
+            if (a < 0 || b > T || (i > 0 && a < (int64_t)seq_start[i - 1] + seq_len[i - 1]))
+                atomicMax(&s_err, 1);
         } else {
-            a = uni * i;
-            b = uni * (i + 1);
+            if (cu_seqlens) {
+                a = cu_seqlens[i];
+                b = cu_seqlens[i + 1];
+            } else {
+                a = uni * i;
+                b = uni * (i + 1);
+            }
+            if (i == 0 && a != 0) atomicMax(&s_err, 1);
+            if (i == B - 1 && b != T) atomicMax(&s_err, 1);
         }
-        if (i == 0 && a != 0) atomicMax(&s_err, 1);
-        if (i == B - 1 && b != T) atomicMax(&s_err, 1);
         if (b < a) atomicMax(&s_err, 1);
         else if (b - a > (int64_t)max_seqlen) atomicMax(&s_err, 2);
         s_start[i] = (int32_t)a;
@@ -174,16 +187,20 @@ size_t schedule_smem_bytes(int B)
     return sizeof(unsigned long long) * (size_t)NP + sizeof(int32_t) * 3 * (size_t)B;
 }
 
-cudaError_t launch_schedule(const int32_t *cu_seqlens, int B, int64_t T, int H, int max_seqlen,
-                            SchedParams sp, WsHeader *hdr, Item *items, int32_t *status, cudaStream_t stream)
+cudaError_t launch_schedule(const int32_t *cu_seqlens, const int32_t *seq_start, const int32_t *seq_len, int B,
+                            int64_t T, int H, int max_seqlen, SchedParams sp, WsHeader *hdr, Item *items,
+                            int32_t *status, cudaStream_t stream)
 {
     const size_t smem = schedule_smem_bytes(B);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    static DeviceOnce once;                              // the limit for the largest B, set once
+    cudaError_t e = once.run([] {
+        return cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)schedule_smem_bytes(VIT_MAX_SEGMENTS));
+    });
+    if (e != cudaSuccess) return e;
     LaunchScope scope("schedule", stream);
-    schedule_kernel<<<1, kThreads, smem, stream>>>(cu_seqlens, B, T, H, max_seqlen, sp, hdr, items, status);
+    schedule_kernel<<<1, kThreads, smem, stream>>>(cu_seqlens, seq_start, seq_len, B, T, H, max_seqlen, sp, hdr,
+                                                   items, status);
     return cudaGetLastError();
 }
 
