@@ -347,9 +347,13 @@ def run_ours(args, rank, world, local):
                         "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside a long step loop)",
                         "algorithmic_flops_per_launch": alg}
         else:
-            if dom == "attn_short":      # q, k, v read and out written once per token it owns
+            tiny_max = min(short_max, 64)
+            if dom == "attn_tiny":       # q, k, v read and out written once per token it owns
                 L = w.lengths
-                alg = 8.0 * float(L[L <= short_max].sum()) * H * D
+                alg = 8.0 * float(L[L <= tiny_max].sum()) * H * D
+            elif dom == "attn_short":
+                L = w.lengths
+                alg = 8.0 * float(L[(L > tiny_max) & (L <= short_max)].sum()) * H * D
             elif dom == "qk_norm_rope":  # q and k (k alone with --fused-q) read and written once
                 alg = (4.0 if args.fused_q else 8.0) * T * H * D
             else:

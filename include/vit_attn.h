@@ -350,8 +350,10 @@ vit_status_t vit_varlen_attn_noalloc(const void *q, const void *k, const void *v
 /*
  * Kernel split of vit_varlen_attn: segments longer than `short_max` tokens run
  * on the tcgen05/TMEM long-segment kernel (256 query rows per work item), the
- * others on the short-segment kernel (128 query rows per item). Default 64, the
- * measured crossover of the two kernels on GB300.
+ * others on warp-MMA kernels: segments of at most min(short_max, 64) tokens on
+ * the tiny-segment kernel (one item per segment and head, the next item loaded
+ * while the current one computes), longer ones on the short-segment kernel
+ * (128 query rows per item). Default 64, the measured crossover on GB300.
  * 0 sends every segment to the long kernel, INT_MAX every segment to the short
  * one; the results agree within the output tolerance either way. Process-wide
  * setting read at each call; returns the previous value.

@@ -14,6 +14,7 @@ namespace vit {
 size_t schedule_smem_bytes(int B);
 int attn_short_bm();
 int attn_long_bm();
+int attn_tiny_max();
 }  // namespace vit
 
 using namespace vit;
@@ -231,6 +232,7 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
     Item *items = reinterpret_cast<Item *>(hdr + 1);
     SchedParams sp;
     sp.short_max = g_short_max.load();
+    sp.tiny_max = sp.short_max < attn_tiny_max() ? sp.short_max : attn_tiny_max();
     sp.bm_long = attn_long_bm();
     sp.bm_short = attn_short_bm();
     cudaError_t e = launch_schedule(padded ? nullptr : cu_seqlens, seq_start, seq_len, B, T, H, max_seqlen, sp, hdr,
@@ -271,7 +273,13 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
         e = launch_attn_long(a, max_items(T, H, B, sp.bm_long), sms, g_stall_v.load(), s);
         if (e != cudaSuccess) return VIT_ERR_CUDA;
     }
-    if (sp.short_max > 0) e = launch_attn_short(a, max_items(T, H, B, sp.bm_short), sms, s);
+    // segments in (tiny_max, short_max] on the short-segment kernel, the rest of the short ones
+    // on the tiny-segment kernel; a kernel is launched only when its class can be non-empty
+    if (sp.short_max > sp.tiny_max) {
+        e = launch_attn_short(a, max_items(T, H, B, sp.bm_short), sms, s);
+        if (e != cudaSuccess) return VIT_ERR_CUDA;
+    }
+    if (sp.tiny_max > 0) e = launch_attn_tiny(a, (int64_t)H * B, sms, s);
     return from_cuda(e);
 }
 

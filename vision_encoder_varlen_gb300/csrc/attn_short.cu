@@ -24,6 +24,7 @@
 // Any segment length works (longer ones loop over 128-key tiles); the
 // long-segment kernel normally takes those.
 #include "internal.h"
+#include "warp_mma.cuh"
 
 namespace vit {
 namespace {
@@ -41,58 +42,13 @@ template <int D> struct ShortCfg {
     static constexpr int MIN_BLOCKS = D <= 32 ? 3 : 2;          // CTAs per SM the register budget allows
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
+using namespace wmma16;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    const int n = valid ? 16 : 0;                                // 0 source bytes -> 16 zero bytes
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
-__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;\n" ::); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-
-__device__ __forceinline__ void mma16816(float *c, const uint32_t *a, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// Copy rows [0, rows) of a tile (row r = token row0 + r) into smem with the padded
-// pitch; rows >= valid_rows are zero-filled and never read from HBM.
+// Copy rows [0, rows) of a tile into shared memory with the padded pitch (zero fill past valid_rows).
 template <int D>
 __device__ __forceinline__ void load_rows(__nv_bfloat16 *s, const __nv_bfloat16 *g, int64_t stride, int64_t row0,
                                           int rows, int valid_rows) {
-    constexpr int CH = D / 8;                                    // 16-byte chunks per row
-    for (int i = threadIdx.x; i < rows * CH; i += kThreads) {
-        const int r = i / CH, c = i - r * CH;
-        const bool ok = r < valid_rows;
-        const __nv_bfloat16 *src = g + (ok ? (row0 + r) * stride : 0) + c * 8;
-        cp_async16(smem_u32(s + r * ShortCfg<D>::PITCH + c * 8), src, ok);
-    }
+    wmma16::load_rows<D, ShortCfg<D>::PITCH, kThreads>(s, g, stride, row0, rows, valid_rows);
 }
 
 template <int D, bool FQ>

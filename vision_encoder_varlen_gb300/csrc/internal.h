@@ -22,17 +22,19 @@ struct WsHeader {
     int32_t n_long;      // items [0, n_long) go to the long-segment kernel
     int32_t n_short;     // items [n_long, n_long + n_short) go to the short-segment kernel
     int32_t bm_long;     // query rows per long item
-    int32_t bm_short;    // query rows per short item
+    int32_t bm_short;    // query rows per short (and tiny) item
     int32_t error;       // device-detected error of the last scheduling pass (0 = none)
-    int32_t pad[11];
+    int32_t n_tiny;      // items [n_long + n_short, + n_tiny) go to the tiny-segment kernel
+    int32_t pad[10];
 };
 static_assert(sizeof(WsHeader) == 64, "header is 64 bytes");
 
 // Scheduling parameters chosen by the host.
 struct SchedParams {
-    int short_max;   // segments with length <= short_max use the short-segment kernel
+    int short_max;   // segments with length <= short_max use a warp-MMA kernel, longer ones the tcgen05 one
+    int tiny_max;    // of those, segments with length <= tiny_max use the tiny-segment kernel
     int bm_long;     // q rows per long item
-    int bm_short;    // q rows per short item
+    int bm_short;    // q rows per short item (a tiny segment is always one item per head)
 };
 
 // Upper bound on the number of items of one class for these sizes.
@@ -109,6 +111,8 @@ struct AttnArgs {
 };
 
 cudaError_t launch_attn_short(const AttnArgs &a, int64_t max_items_short, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_attn_tiny(const AttnArgs &a, int64_t max_items_tiny, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_attn_long(const AttnArgs &a, int64_t max_items_long, int num_sms, int stall_v,
                              cudaStream_t stream);

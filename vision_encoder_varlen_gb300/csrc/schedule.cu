@@ -14,7 +14,10 @@
 //      (length desc, index asc) keys, so the order is deterministic;
 //   3. expands every segment into (segment, head, q-block) work items: long
 //      segments into blocks of bm_long query rows for the long-segment kernel,
-//      short ones into blocks of bm_short rows for the short-segment kernel.
+//      short ones into blocks of bm_short rows for the short-segment kernel,
+//      tiny ones (at most tiny_max tokens) into one item per head for the
+//      tiny-segment kernel. Longest first, the three classes come out as three
+//      contiguous runs of the item list.
 //      Items never straddle two segments; the q-block is the fastest index,
 //      so concurrently running CTAs share one head's K/V in L2.
 // On invalid offsets it records the error and publishes zero items, so the
@@ -102,6 +105,7 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
         if (tid == 0) {
             hdr->n_long = 0;
             hdr->n_short = 0;
+            hdr->n_tiny = 0;
             hdr->error = s_err == 1 ? VIT_ERR_BAD_SEQLENS : VIT_ERR_SEQLEN_EXCEEDS_MAX;
             report_error(status, hdr->error);
         }
@@ -133,7 +137,7 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
     // ---- 3. item counts per sorted position, exclusive scan, expansion
     const int per = (B + kThreads - 1) / kThreads;
     const int lo = min(tid * per, B), hi = min(lo + per, B);
-    int64_t local = 0, local_long = 0;
+    int64_t local = 0, local_long = 0, local_tiny = 0;
     for (int p = lo; p < hi; ++p) {
         const int seg = (int)(s_key[p] & 0xffffffffu);
         const int len = s_len[seg];
@@ -142,10 +146,12 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
         const int64_t n = (int64_t)H * ((len + bm - 1) / bm);
         local += n;
         if (is_long) local_long += n;
+        else if (len <= sp.tiny_max) local_tiny += n;
     }
-    int64_t total, total_long;
+    int64_t total, total_long, total_tiny;
     int64_t run = block_exclusive_scan(local, s_warp, &total);
     block_exclusive_scan(local_long, s_warp, &total_long);
+    block_exclusive_scan(local_tiny, s_warp, &total_tiny);
     for (int p = lo; p < hi; ++p) {
         const int seg = (int)(s_key[p] & 0xffffffffu);
         const int len = s_len[seg];
@@ -171,7 +177,8 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
     }
     if (tid == 0) {
         hdr->n_long = (int32_t)total_long;
-        hdr->n_short = (int32_t)(total - total_long);
+        hdr->n_short = (int32_t)(total - total_long - total_tiny);
+        hdr->n_tiny = (int32_t)total_tiny;
         hdr->bm_long = sp.bm_long;
         hdr->bm_short = sp.bm_short;
         hdr->error = 0;
