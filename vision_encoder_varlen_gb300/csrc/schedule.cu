@@ -10,8 +10,12 @@
 //      sequence_lengths describe) is taken instead when seq_len is given:
 //      starts ascending, segments inside [0, T) and not overlapping; the rows
 //      between them are padding that nothing reads or writes;
-//   2. orders segments longest first (LPT) with a bitonic sort of
-//      (length desc, index asc) keys, so the order is deterministic;
+//   2. orders the segments: those for the long-segment kernel longest first
+//      (LPT, a bitonic sort of (length desc, index asc) keys, so the order is
+//      deterministic and the persistent CTAs end together), then the short
+//      and the tiny ones in index order (a stable partition by block scans:
+//      their items are small, so sorting them buys no balance and cost most of
+//      the scheduler's time for thousands of small images);
 //   3. expands every segment into (segment, head, q-block) work items: long
 //      segments into blocks of bm_long query rows for the long-segment kernel,
 //      short ones into blocks of bm_short rows for the short-segment kernel,
@@ -61,7 +65,7 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
                 const int32_t *__restrict__ seq_len, int B, int64_t T, int H, int max_seqlen,
                 SchedParams sp, WsHeader *hdr, Item *items, int32_t *status)
 {
-    extern __shared__ unsigned long long s_key[];      // [NP] sort keys, then [B] int32 offsets reuse
+    extern __shared__ unsigned long long s_key[];      // [NP] sort keys of the long segments
     __shared__ int64_t s_warp[32];
     __shared__ int s_err;
     const int tid = threadIdx.x;
@@ -69,7 +73,8 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
     while (NP < B) NP <<= 1;
     int32_t *s_start = reinterpret_cast<int32_t *>(s_key + NP);   // [B] segment start by segment index
     int32_t *s_len = s_start + B;                                  // [B] segment length by segment index
-    int32_t *s_off = s_len + B;                                    // [B] first item of sorted position p
+    int32_t *s_off = s_len + B;                                    // [B] first item of position p
+    int32_t *s_order = s_off + B;                                  // [B] segment index at position p
 
     if (tid == 0) s_err = 0;
     __syncthreads();
@@ -112,34 +117,52 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
         return;
     }
 
-    // ---- 2. LPT order: ascending keys = descending length, then ascending index
-    for (int i = tid; i < NP; i += kThreads)
-        s_key[i] = i < B ? ((unsigned long long)(0x7fffffffu - (uint32_t)s_len[i]) << 32) | (uint32_t)i
-                         : ~0ull;
+    // ---- 2. order: long class longest first, then short, then tiny (index order within each)
+    const int per = (B + kThreads - 1) / kThreads;
+    const int lo = min(tid * per, B), hi = min(lo + per, B);
+    auto seg_class = [&](int len) { return len > sp.short_max ? 0 : (len <= sp.tiny_max ? 2 : 1); };
+    int64_t cnt[3] = {0, 0, 0};
+    for (int i = lo; i < hi; ++i) ++cnt[seg_class(s_len[i])];
+    int64_t tot[3];
+    int64_t pos[3];
+    for (int c = 0; c < 3; ++c) pos[c] = block_exclusive_scan(cnt[c], s_warp, &tot[c]);
+    const int n_lseg = (int)tot[0];
+    pos[1] += tot[0];
+    pos[2] += tot[0] + tot[1];
+    for (int i = lo; i < hi; ++i) {
+        const int c = seg_class(s_len[i]);
+        if (c == 0)      // ascending keys = descending length, then ascending index
+            s_key[pos[0]++] = ((unsigned long long)(0x7fffffffu - (uint32_t)s_len[i]) << 32) | (uint32_t)i;
+        else
+            s_order[pos[c]++] = i;
+    }
+    int NPL = 1;
+    while (NPL < n_lseg) NPL <<= 1;
+    for (int i = n_lseg + tid; i < NPL; i += kThreads) s_key[i] = ~0ull;
     __syncthreads();
-    for (int k = 2; k <= NP; k <<= 1) {
+    for (int k = 2; k <= NPL; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < NP; i += kThreads) {
+            for (int i = tid; i < NPL; i += kThreads) {
                 const int l = i ^ j;
                 if (l > i) {
-                    const unsigned long long a = s_key[i], b = s_key[l];
+                    const unsigned long long x = s_key[i], y = s_key[l];
                     const bool up = (i & k) == 0;
-                    if ((a > b) == up) {
-                        s_key[i] = b;
-                        s_key[l] = a;
+                    if ((x > y) == up) {
+                        s_key[i] = y;
+                        s_key[l] = x;
                     }
                 }
             }
             __syncthreads();
         }
     }
+    for (int p = tid; p < n_lseg; p += kThreads) s_order[p] = (int32_t)(s_key[p] & 0xffffffffu);
+    __syncthreads();
 
-    // ---- 3. item counts per sorted position, exclusive scan, expansion
-    const int per = (B + kThreads - 1) / kThreads;
-    const int lo = min(tid * per, B), hi = min(lo + per, B);
+    // ---- 3. item counts per position, exclusive scan, expansion
     int64_t local = 0, local_long = 0, local_tiny = 0;
     for (int p = lo; p < hi; ++p) {
-        const int seg = (int)(s_key[p] & 0xffffffffu);
+        const int seg = s_order[p];
         const int len = s_len[seg];
         const bool is_long = len > sp.short_max;
         const int bm = is_long ? sp.bm_long : sp.bm_short;
@@ -153,7 +176,7 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
     block_exclusive_scan(local_long, s_warp, &total_long);
     block_exclusive_scan(local_tiny, s_warp, &total_tiny);
     for (int p = lo; p < hi; ++p) {
-        const int seg = (int)(s_key[p] & 0xffffffffu);
+        const int seg = s_order[p];
         const int len = s_len[seg];
         const int bm = len > sp.short_max ? sp.bm_long : sp.bm_short;
         s_off[p] = (int32_t)run;
@@ -163,7 +186,7 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
     // one warp per sorted segment (a whole-block loop over B segments would leave most threads idle)
     const int lane = tid & 31, warp = tid >> 5;
     for (int p = warp; p < B; p += kThreads / 32) {
-        const int seg = (int)(s_key[p] & 0xffffffffu);
+        const int seg = s_order[p];
         const int len = s_len[seg];
         if (len == 0) continue;
         const int bm = len > sp.short_max ? sp.bm_long : sp.bm_short;
@@ -191,7 +214,7 @@ size_t schedule_smem_bytes(int B)
 {
     int NP = 1;
     while (NP < B) NP <<= 1;
-    return sizeof(unsigned long long) * (size_t)NP + sizeof(int32_t) * 3 * (size_t)B;
+    return sizeof(unsigned long long) * (size_t)NP + sizeof(int32_t) * 4 * (size_t)B;
 }
 
 cudaError_t launch_schedule(const int32_t *cu_seqlens, const int32_t *seq_start, const int32_t *seq_len, int B,
