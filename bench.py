@@ -164,21 +164,77 @@ class Path:
                         status=self.status, lse=self.lse)
 
 
-def e2e_step(vit, w, host, device, stream, fused_q=False):
-    """Through the public API from pinned host buffers: H2D inputs, the calls, D2H output."""
-    grid = host["grid"].to(device, non_blocking=True)
-    q = host["q"].to(device, non_blocking=True)
-    k = host["k"].to(device, non_blocking=True)
-    v = host["v"].to(device, non_blocking=True)
-    nw = host["nw"].to(device, non_blocking=True) if host["nw"] is not None else None
-    inv_freq, pos, cu = vit.rope_freqs(grid, w.total_tokens, w.head_dim, w.theta)
-    if fused_q:
-        cs = vit.rope_table(inv_freq, w.head_dim, int(w.grid_hw.max()))
-        out = vit.encoder_attn(q, k, v, cu, w.max_seqlen, pos, inv_freq, cs, nw, w.eps, k_out=k)
-    else:
-        qr, kr = vit.qk_norm_rope(q, k, pos, inv_freq, nw, w.eps, inplace=True)
-        out = vit.varlen_attn(qr, kr, v, cu, w.max_seqlen)
-    host["out"].copy_(out, non_blocking=True)
+class E2EPipeline:
+    """The path as a serving loop runs it, through the public API from pinned host buffers: every
+    step uploads its inputs (q, k, v, the grid list, the norm weights) and downloads its output.
+    Uploads go on one copy stream and downloads on another, into two sets of device buffers, so
+    step i+1's inputs travel up and step i's output travels down while a step computes. (Three
+    upload streams measured the same: the host link, not one copy engine, is the limit.)"""
+
+    def __init__(self, vit, w, host, device, fused_q=False):
+        self.vit, self.w, self.host, self.fused_q = vit, w, host, fused_q
+        T, H, D, B = w.total_tokens, w.heads, w.head_dim, w.num_segments
+        self.up = torch.cuda.Stream(device)
+        self.down = torch.cuda.Stream(device)
+        self.bufs = []
+        for _ in range(2):
+            self.bufs.append({
+                "grid": torch.empty_like(host["grid"], device=device),
+                "q": torch.empty((T, H, D), dtype=torch.bfloat16, device=device),
+                "k": torch.empty((T, H, D), dtype=torch.bfloat16, device=device),
+                "v": torch.empty((T, H, D), dtype=torch.bfloat16, device=device),
+                "nw": torch.empty_like(host["nw"], device=device) if host["nw"] is not None else None,
+                "out": torch.empty((T, H, D), dtype=torch.bfloat16, device=device),
+                "ws": torch.empty(vit.workspace_size(T, H, B, D), dtype=torch.uint8, device=device),
+                "uploaded": torch.cuda.Event(), "consumed": torch.cuda.Event(), "downloaded": torch.cuda.Event(),
+                "used": False,
+            })
+
+    def _upload(self, b):
+        buf, host = self.bufs[b], self.host
+        with torch.cuda.stream(self.up):
+            if buf["used"]:
+                self.up.wait_event(buf["consumed"])          # the step that last read these inputs is done
+            for name in ("grid", "q", "k", "v", "nw"):
+                if buf[name] is not None:
+                    buf[name].copy_(host[name], non_blocking=True)
+            buf["uploaded"].record(self.up)
+
+    def _compute(self, b):
+        vit, w, buf = self.vit, self.w, self.bufs[b]
+        cur = torch.cuda.current_stream()
+        cur.wait_event(buf["uploaded"])
+        if buf["used"]:
+            cur.wait_event(buf["downloaded"])                # this buffer's previous output has left
+        inv_freq, pos, cu = vit.rope_freqs(buf["grid"], w.total_tokens, w.head_dim, w.theta)
+        if self.fused_q:
+            cs = vit.rope_table(inv_freq, w.head_dim, int(w.grid_hw.max()))
+            vit.encoder_attn(buf["q"], buf["k"], buf["v"], cu, w.max_seqlen, pos, inv_freq, cs, buf["nw"], w.eps,
+                             k_out=buf["k"], out=buf["out"], workspace=buf["ws"])
+        else:
+            vit.qk_norm_rope(buf["q"], buf["k"], pos, inv_freq, buf["nw"], w.eps, inplace=True)
+            vit.varlen_attn(buf["q"], buf["k"], buf["v"], cu, w.max_seqlen, out=buf["out"], workspace=buf["ws"])
+        buf["consumed"].record(cur)
+        buf["used"] = True
+
+    def _download(self, b):
+        buf = self.bufs[b]
+        with torch.cuda.stream(self.down):
+            self.down.wait_event(buf["consumed"])
+            self.host["out"].copy_(buf["out"], non_blocking=True)
+            buf["downloaded"].record(self.down)
+
+    def run(self, steps: int, start_event=None):
+        """Enqueue `steps` steps; the current stream waits for the last download at the end."""
+        if start_event is not None:
+            self.up.wait_event(start_event)
+        self._upload(0)
+        for i in range(steps):
+            if i + 1 < steps:
+                self._upload((i + 1) % 2)
+            self._compute(i % 2)
+            self._download(i % 2)
+        torch.cuda.current_stream().wait_event(self.bufs[(steps - 1) % 2]["downloaded"])
 
 
 def load_traffic(kernel: str, workload: str):
@@ -310,20 +366,20 @@ def run_ours(args, rank, world, local):
                 "out": torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory()}
         h2d = 3 * tensor_bytes + host["grid"].numel() * 4 + (host["nw"].numel() * 2 if host["nw"] is not None else 0)
         d2h = tensor_bytes
-        for _ in range(2):
-            e2e_step(vit, w, host, device, stream, args.fused_q)
+        pipe = E2EPipeline(vit, w, host, device, args.fused_q)
+        pipe.run(3)                                          # warm-up
         torch.cuda.synchronize()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e2e_steps = max(1, min(args.steps, 10))
+        e2e_steps = max(2, min(args.steps, 10))
         e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step(vit, w, host, device, stream, args.fused_q)
+        pipe.run(e2e_steps, start_event=e0)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, device)
         e2e = {"value": job_tflops(w.useful_flops, world, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "overlap": "step i+1's upload and step i's download on two copy streams run during compute"}
 
     if rank != 0:
         return
