@@ -462,7 +462,7 @@ def run_split_sweep(args):
                 ws = torch.empty(vit.workspace_size(T, 16, w.num_segments, D), dtype=torch.uint8, device="cuda")
                 out = torch.empty_like(q)
                 res = {}
-                for name, sm in (("short_kernel_ms", 1 << 30), ("tcgen05_kernel_ms", 0)):
+                for name, sm in (("warp_mma_kernels_ms", 1 << 30), ("tcgen05_kernel_ms", 0)):
                     vit.set_short_segment_max(sm)
                     for _ in range(args.warmup):
                         vit.varlen_attn(q, k, v, cu, 4096, out=out, workspace=ws)
