@@ -156,6 +156,10 @@ enum {
  * Arguments as for vit_qk_norm_rope, plus:
  *   rope_mode   VIT_ROPE_ROTATE_HALF or VIT_ROPE_INTERLEAVED (else
  *               VIT_ERR_BAD_ARGUMENT).
+ *   status_dev  device int32 [1] or NULL (see conventions): rows may move
+ *               through shared memory with bulk copies whose waits are
+ *               bounded; one that expires stores VIT_ERR_TIMEOUT. (The plain
+ *               vit_qk_norm_rope passes NULL.)
  * In both calls either half may be left out: q_in and q_out both NULL skip q
  * (its strides are then ignored), k_in and k_out both NULL skip k. Passing
  * only one pointer of a pair, or leaving out both halves, is
@@ -166,7 +170,8 @@ vit_status_t vit_qk_norm_rope_ex(const void *q_in, void *q_out, const void *k_in
                                  int64_t q_in_stride, int64_t q_out_stride,
                                  int64_t k_in_stride, int64_t k_out_stride,
                                  const int32_t *pos_hw, const float *inv_freq,
-                                 const void *norm_w, float eps, int rope_mode, vit_stream_t stream);
+                                 const void *norm_w, float eps, int rope_mode, int32_t *status_dev,
+                                 vit_stream_t stream);
 
 /*
  * Rotary cos/sin table over positions, for the attention call that rotates Q

@@ -114,7 +114,7 @@ def test_extended_calls_validation_without_gpu(L):
         a = dict(good, **kw)
         return ex(p(a["qi"]) if a["qi"] else None, p(a["qo"]) if a["qo"] else None,
                   p(a["ki"]) if a["ki"] else None, p(a["ko"]) if a["ko"] else None, 10, 2, 80, 160, 160, 160, 160,
-                  p(16), p(16), None, 1e-6, a["mode"], None)
+                  p(16), p(16), None, 1e-6, a["mode"], None, None)
     assert call(mode=2) == -14                       # unknown rotary pairing
     assert call(mode=-1) == -14
     assert call(qo=0) == -1                          # half a q pair

@@ -59,7 +59,7 @@ def lib() -> ctypes.CDLL:
             L.vit_rope_freqs.argtypes = [i32, f32, vp, i32, i64, vp, vp, vp, vp, vp]
             L.vit_qk_norm_rope.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i64, i64, vp, vp, vp, f32, vp]
             L.vit_qk_norm_rope_ex.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i64, i64, vp, vp, vp, f32,
-                                              i32, vp]
+                                              i32, vp, vp]
             L.vit_varlen_attn_workspace_size.restype = sz
             L.vit_varlen_attn_workspace_size.argtypes = [i64, i32, i32, i32]
             L.vit_varlen_attn.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, vp, i32, i32, f32, vp, i64, vp,
@@ -164,7 +164,8 @@ ROPE_INTERLEAVED = 1    # pairs (2m, 2m + 1), the "complex_rope" mode
 
 def qk_norm_rope(q: torch.Tensor | None, k: torch.Tensor | None, pos_hw: torch.Tensor, inv_freq: torch.Tensor,
                  norm_w: torch.Tensor | None = None, eps: float = 1e-6, *, q_out: torch.Tensor | None = None,
-                 k_out: torch.Tensor | None = None, inplace: bool = False, interleaved: bool = False, stream=None):
+                 k_out: torch.Tensor | None = None, inplace: bool = False, interleaved: bool = False,
+                 status: torch.Tensor | None = None, stream=None):
     """QK-RMSNorm (if norm_w [2, D] is given) + 2D RoPE. Returns (q', k'); a half passed as None is
     skipped and returned as None. ``interleaved`` rotates adjacent pairs instead of (m, m + D/2)."""
     ref = q if q is not None else k
@@ -192,7 +193,8 @@ def qk_norm_rope(q: torch.Tensor | None, k: torch.Tensor | None, pos_hw: torch.T
         raise ValueError("norm_w must be a contiguous bfloat16 tensor [2, D]")
     mode = ROPE_INTERLEAVED if interleaved else ROPE_ROTATE_HALF
     _check(lib().vit_qk_norm_rope_ex(_ptr(q), _ptr(q_out), _ptr(k), _ptr(k_out), T, H, D, qs, qos, ks, kos,
-                                     _ptr(pos_hw), _ptr(inv_freq), _ptr(norm_w), float(eps), mode, _stream(stream)),
+                                     _ptr(pos_hw), _ptr(inv_freq), _ptr(norm_w), float(eps), mode, _ptr(status),
+                                     _stream(stream)),
            "vit_qk_norm_rope_ex")
     return q_out, k_out
 

@@ -118,7 +118,8 @@ vit_status_t vit_rope_freqs(int dim, float theta, const int32_t *grid_hw, int n_
 vit_status_t vit_qk_norm_rope_ex(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T, int H,
                                  int D, int64_t q_in_stride, int64_t q_out_stride, int64_t k_in_stride,
                                  int64_t k_out_stride, const int32_t *pos_hw, const float *inv_freq,
-                                 const void *norm_w, float eps, int rope_mode, vit_stream_t stream)
+                                 const void *norm_w, float eps, int rope_mode, int32_t *status_dev,
+                                 vit_stream_t stream)
 {
     if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
     if (T < 0 || T >= kMaxTokens || H < 1) return VIT_ERR_BAD_SHAPE;
@@ -144,7 +145,7 @@ vit_status_t vit_qk_norm_rope_ex(const void *q_in, void *q_out, const void *k_in
     if (st != VIT_OK) return st;
     return from_cuda(launch_qk_norm_rope(q_in, q_out, k_in, k_out, T, H, D, q_in_stride, q_out_stride, k_in_stride,
                                          k_out_stride, pos_hw, inv_freq, norm_w, eps,
-                                         rope_mode == VIT_ROPE_INTERLEAVED, sms, (cudaStream_t)stream));
+                                         rope_mode == VIT_ROPE_INTERLEAVED, sms, status_dev, (cudaStream_t)stream));
 }
 
 vit_status_t vit_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T, int H, int D,
@@ -153,7 +154,7 @@ vit_status_t vit_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, v
                               vit_stream_t stream)
 {
     return vit_qk_norm_rope_ex(q_in, q_out, k_in, k_out, T, H, D, q_in_stride, q_out_stride, k_in_stride,
-                               k_out_stride, pos_hw, inv_freq, norm_w, eps, VIT_ROPE_ROTATE_HALF, stream);
+                               k_out_stride, pos_hw, inv_freq, norm_w, eps, VIT_ROPE_ROTATE_HALF, nullptr, stream);
 }
 
 vit_status_t vit_rope_table(const float *inv_freq, int head_dim, int max_pos, float *cos_sin, vit_stream_t stream)

@@ -86,7 +86,7 @@ cudaError_t launch_qk_norm_rope(const void *q_in, void *q_out, const void *k_in,
                                 int H, int D, int64_t q_in_stride, int64_t q_out_stride,
                                 int64_t k_in_stride, int64_t k_out_stride, const int32_t *pos_hw,
                                 const float *inv_freq, const void *norm_w, float eps, bool interleaved,
-                                int num_sms, cudaStream_t stream);
+                                int num_sms, int32_t *status, cudaStream_t stream);
 
 // segments from cu_seqlens (contiguous; NULL = B uniform segments) or, when seq_len is
 // given, from per-segment starts and lengths (a padded layout)
