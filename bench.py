@@ -63,6 +63,12 @@ def reduce_max(x: float, device) -> float:
     return float(t.item())
 
 
+def rank_inputs(w: wl.Workload, rank: int) -> dict:
+    """This rank's shard of the job: a batch of the workload's shape with its own seeded values,
+    so N ranks process N different batches (weak scaling, no exchange between ranks)."""
+    return w.tensors(seed_offset=rank)
+
+
 def job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
     """Whole-job throughput: every rank's useful flops over the slowest rank's step time."""
     return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
@@ -304,7 +310,7 @@ def run_ours(args, rank, world, local):
     if args.short_max is not None:
         vit.set_short_segment_max(args.short_max)
     w = wl.make_config(args.config)
-    t = w.tensors()
+    t = rank_inputs(w, rank)
     T, H, D = w.total_tokens, w.heads, w.head_dim
     path = Path(vit, w, t, device, lse=args.lse, interleaved=args.interleaved, fused_q=args.fused_q)
     stream = torch.cuda.current_stream()
@@ -428,7 +434,8 @@ def run_ours(args, rank, world, local):
                    "q_prologue": "fused into the attention Q load" if args.fused_q else "separate pass",
                    "l2": "L2 flushed between steps" if flush else
                    f"inputs larger than L2 ({working_set / 2 ** 20:.0f} MiB working set)",
-                   "parallelism": "replicas" if world > 1 else "single"},
+                   "parallelism": f"data-parallel over {world} ranks, one batch each, no exchange" if world > 1
+                   else "single"},
         "tokens_per_s": T * world / (ms * 1e-3),
         "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
         "clocks": clk,

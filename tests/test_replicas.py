@@ -1,6 +1,8 @@
 """Multi-rank host logic of the benchmark (gloo, world size 2, CPU): the
-max-over-ranks timing, the whole-job value, and the reference arm printing
-only on rank 0. The data path itself has no collective (replicas only)."""
+max-over-ranks timing, the whole-job value, each rank's own batch, and the
+reference arm printing only on rank 0. The data path itself has no
+collective: (segment, head) units are independent, so ranks shard the job by
+batches."""
 import argparse
 import io
 import os
@@ -60,3 +62,12 @@ def test_reference_arm_is_silent_off_rank_zero():
     with contextlib.redirect_stdout(buf):
         bench.run_reference(args, rank=1, world=2)
     assert buf.getvalue() == ""
+
+
+def test_each_rank_processes_its_own_batch():
+    from vision_encoder_varlen_gb300 import workloads as wl
+    w = wl.make_config(1)
+    a, b = bench.rank_inputs(w, 0), bench.rank_inputs(w, 1)
+    assert a["q"].shape == b["q"].shape
+    assert not torch.equal(a["q"], b["q"]) and not torch.equal(a["v"], b["v"])
+    assert torch.equal(bench.rank_inputs(w, 1)["k"], b["k"])          # seeded: the same every run
