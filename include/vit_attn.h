@@ -197,7 +197,9 @@ vit_status_t vit_rope_table(const float *inv_freq, int head_dim, int max_pos, fl
 
 /*
  * Workspace bytes vit_varlen_attn needs for these sizes (an upper bound
- * independent of the segment lengths). Returns 0 for invalid sizes.
+ * independent of the segment lengths). Returns 0 for invalid sizes, including
+ * sizes whose work list could exceed 2^31 - 1 items (H * (T/64 + B)); the
+ * attention calls then return VIT_ERR_BAD_SHAPE.
  */
 size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D);
 

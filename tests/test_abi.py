@@ -53,6 +53,8 @@ def test_workspace_size_bounds(L):
     assert vit.workspace_size(100, 4, 2, 81) == 0        # bad head_dim
     assert vit.workspace_size(100, 0, 2, 80) == 0        # no heads
     assert vit.workspace_size(100, 4, 8193, 80) == 0     # too many segments
+    assert vit.workspace_size(2 ** 31 - 1, 64, 1, 80) == 0   # work list past 2^31 items
+    assert vit.workspace_size(2 ** 31 - 1, 63, 1, 80) > 0
 
 
 def _attn(L, **kw):

@@ -172,8 +172,9 @@ size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D)
 {
     if (T < 0 || T >= kMaxTokens || H < 1 || B < 0 || B > VIT_MAX_SEGMENTS || !head_dim_ok(D)) return 0;
     // every work item covers at least 64 query rows (128 for short segments, 256 for long
-    // ones), so this bound holds for any kernel split
+    // ones), so this bound holds for any kernel split; item indices are int32 on the device
     const int64_t items = max_items(T, H, B, 64);
+    if (items >= ((int64_t)1 << 31)) return 0;
     return sizeof(WsHeader) + sizeof(Item) * (size_t)items;
 }
 
