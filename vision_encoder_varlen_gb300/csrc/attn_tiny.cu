@@ -10,9 +10,10 @@
 // 4 * L^2 * D flops: about L / 2 flops per byte, so it is bound by HBM and by
 // latency, not by arithmetic. The design therefore keeps many bytes in flight:
 //   - one work item = one (segment, head): Q, K and V are at most 64 rows;
-//   - each CTA (4 warps) holds two items in shared memory and loads the next
-//     item with cp.async while it computes the current one; small tiles let
-//     three CTAs share an SM;
+//   - each CTA (4 warps) holds two items' K and V in shared memory and loads
+//     the next item with cp.async while it computes the current one; each
+//     warp takes its 16 query rows straight from HBM into MMA fragments, so
+//     four CTAs share an SM;
 //   - warp w owns query rows [16w, 16w + 16) as one MMA tile; the whole key
 //     range is one tile, so the softmax is a single pass (exact row max, no
 //     running rescale);
@@ -30,36 +31,40 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int TM = 64;                       // rows of Q, K and V per item (segment length bound)
 
-template <int D> struct TinyCfg {
+// Shared memory holds K and V of two items; Q goes straight from HBM into each warp's MMA
+// fragments (16 rows per warp), except when Q arrives raw and is rotated in shared memory (FQ).
+template <int D, bool FQ> struct TinyCfg {
     static constexpr int PITCH = D + 8;                          // padded row pitch: conflict-free ldmatrix
-    static constexpr int MIN_BLOCKS = D <= 96 ? 3 : 2;          // CTAs per SM the shared memory allows
     static constexpr int TILE = TM * PITCH;                      // elements of one 64-row tile
-    static constexpr int BUF = 3 * TILE;                         // Q, K, V of one item
+    static constexpr int NT = FQ ? 3 : 2;                        // tiles per item: (Q,) K, V
+    static constexpr int BUF = NT * TILE;
     static constexpr size_t SMEM = sizeof(__nv_bfloat16) * 2 * BUF;   // two items
+    // CTAs per SM: shared memory, then registers (at most 128 per thread for four)
+    static constexpr int MIN_BLOCKS = (!FQ && D <= 96) ? 4 : (D <= 96 ? 3 : 2);
 };
 
-template <int D>
+template <int D, bool FQ>
 __device__ __forceinline__ void load_item(__nv_bfloat16 *buf, const Item &item, const __nv_bfloat16 *q,
                                           const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t qs, int64_t ks,
                                           int64_t vs) {
-    using C = TinyCfg<D>;
+    using C = TinyCfg<D, FQ>;
     const int L = item.y, rows = (L + 15) & ~15;
     const int64_t row0 = item.x;
     const int64_t hoff = (int64_t)item.w * D;
-    load_rows<D, C::PITCH, kThreads>(buf, q + hoff, qs, row0, rows, L);
-    load_rows<D, C::PITCH, kThreads>(buf + C::TILE, k + hoff, ks, row0, rows, L);
-    load_rows<D, C::PITCH, kThreads>(buf + 2 * C::TILE, v + hoff, vs, row0, rows, L);
+    if constexpr (FQ) load_rows<D, C::PITCH, kThreads>(buf + 2 * C::TILE, q + hoff, qs, row0, rows, L);
+    load_rows<D, C::PITCH, kThreads>(buf, k + hoff, ks, row0, rows, L);
+    load_rows<D, C::PITCH, kThreads>(buf + C::TILE, v + hoff, vs, row0, rows, L);
 }
 
 template <int D, bool FQ>
-__global__ void __launch_bounds__(kThreads, TinyCfg<D>::MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, TinyCfg<D, FQ>::MIN_BLOCKS)
 attn_tiny_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                  const __nv_bfloat16 *__restrict__ v, int64_t q_stride, int64_t k_stride, int64_t v_stride,
                  __nv_bfloat16 *__restrict__ out, int64_t out_stride, float *__restrict__ lse, int H,
                  float scale_log2, const WsHeader *__restrict__ hdr, const Item *__restrict__ items,
                  const rope::QRope qr)
 {
-    using C = TinyCfg<D>;
+    using C = TinyCfg<D, FQ>;
     constexpr int PITCH = C::PITCH;
     constexpr int KSTEPS = D / 16;       // QK^T reduction steps
     constexpr int DN = D / 8;            // output n-blocks of 8 columns
@@ -72,21 +77,37 @@ attn_tiny_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
     const int r_base = warp * 16;
 
     int it = blockIdx.x;
-    if (it < n_items) load_item<D>(smem, items[first + it], q, k, v, q_stride, k_stride, v_stride);
+    if (it < n_items) load_item<D, FQ>(smem, items[first + it], q, k, v, q_stride, k_stride, v_stride);
     cp_async_commit();
     for (int n = 0; it < n_items; ++n, it += gridDim.x) {
         // the next item goes into the other buffer while this one is computed; that buffer's
         // previous item finished before the barrier that closed the last iteration
         const int nxt = it + gridDim.x;
         if (nxt < n_items)
-            load_item<D>(smem + ((n + 1) & 1) * C::BUF, items[first + nxt], q, k, v, q_stride, k_stride, v_stride);
+            load_item<D, FQ>(smem + ((n + 1) & 1) * C::BUF, items[first + nxt], q, k, v, q_stride, k_stride,
+                             v_stride);
         cp_async_commit();
+        const Item item = items[first + it];
+        const int seg0 = item.x, L = item.y, head = item.w;
+        // this warp's 16 query rows as MMA A fragments, loaded while K and V land: fragment e of
+        // k-step kk holds row g (e even) or g + 8, columns 2 tig, 2 tig + 1 (+ 8 for e >= 2)
+        uint32_t qa[KSTEPS][4];
+        if constexpr (!FQ) {
+            const __nv_bfloat16 *q0r = q + (int64_t)(seg0 + r_base + g) * q_stride + (int64_t)head * D + 2 * tig;
+            const __nv_bfloat16 *q8r = q0r + 8 * q_stride;
+            const bool ok0 = r_base + g < L, ok8 = r_base + g + 8 < L;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                qa[kk][0] = ok0 ? *reinterpret_cast<const uint32_t *>(q0r + kk * 16) : 0u;
+                qa[kk][1] = ok8 ? *reinterpret_cast<const uint32_t *>(q8r + kk * 16) : 0u;
+                qa[kk][2] = ok0 ? *reinterpret_cast<const uint32_t *>(q0r + kk * 16 + 8) : 0u;
+                qa[kk][3] = ok8 ? *reinterpret_cast<const uint32_t *>(q8r + kk * 16 + 8) : 0u;
+            }
+        }
         cp_async_wait_one();                                 // this item's group has landed
         __syncthreads();
 
-        const Item item = items[first + it];
-        const int seg0 = item.x, L = item.y, head = item.w;
-        __nv_bfloat16 *sQ = smem + (n & 1) * C::BUF, *sK = sQ + C::TILE, *sV = sK + C::TILE;
+        __nv_bfloat16 *sK = smem + (n & 1) * C::BUF, *sV = sK + C::TILE, *sQ = sV + C::TILE;
         if constexpr (FQ) {
             // raw Q: thread r normalises and rotates row r (the prologue kernel's arithmetic)
             const int r = threadIdx.x;
@@ -106,8 +127,16 @@ attn_tiny_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
                 uint32_t a[4];
-                ldsm_x4(smem_u32(sQ + (r_base + (lane & 7) + ((lane >> 3) & 1) * 8) * PITCH + kk * 16 + (lane >> 4) * 8),
-                        a[0], a[1], a[2], a[3]);
+                if constexpr (FQ) {
+                    ldsm_x4(smem_u32(sQ + (r_base + (lane & 7) + ((lane >> 3) & 1) * 8) * PITCH + kk * 16 +
+                                     (lane >> 4) * 8),
+                            a[0], a[1], a[2], a[3]);
+                } else {
+                    a[0] = qa[kk][0];
+                    a[1] = qa[kk][1];
+                    a[2] = qa[kk][2];
+                    a[3] = qa[kk][3];
+                }
 #pragma unroll
                 for (int np = 0; np < 4; ++np) {
                     if (np < n16) {
@@ -200,8 +229,8 @@ attn_tiny_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__res
 template <int D>
 cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, cudaStream_t stream)
 {
-    constexpr size_t smem = TinyCfg<D>::SMEM;
-    static_assert(smem <= 227 * 1024, "shared memory budget");
+    const size_t smem = a.fuse_q ? TinyCfg<D, true>::SMEM : TinyCfg<D, false>::SMEM;
+    static_assert(TinyCfg<D, true>::SMEM <= 227 * 1024, "shared memory budget");
     auto kern = a.fuse_q ? attn_tiny_kernel<D, true> : attn_tiny_kernel<D, false>;
     static DeviceOnce once[2];                           // per fused-Q variant
     static int per_sm_of[2][64];                         // resident CTAs per SM, per variant and device
