@@ -1,0 +1,56 @@
+"""Host-side pieces of the benchmark that need no GPU: the algorithmic work the
+roofline divides by, the traffic lookup from the committed ncu summary (and
+its refusal once the kernel source has changed), and the peak fallback."""
+import hashlib
+import json
+import os
+
+import numpy as np
+import pytest
+
+import bench
+from vision_encoder_varlen_gb300 import workloads as wl
+
+
+def test_algorithmic_flops_split_by_kernel():
+    w = wl.make_config(5)
+    L = w.lengths.astype(np.float64)
+    total = bench.kernel_algorithmic_flops(w, "attn_long", 0)
+    assert total == pytest.approx(w.useful_flops)                 # split 0: every segment is long
+    assert total == pytest.approx(4 * np.sum(L * L) * 16 * 80)
+    long64 = bench.kernel_algorithmic_flops(w, "attn_long", 64)
+    short64 = bench.kernel_algorithmic_flops(w, "attn_tiny", 64)
+    assert long64 + short64 == pytest.approx(total)
+    w7 = wl.make_config(7)
+    assert bench.kernel_algorithmic_flops(w7, "attn_long", 64) == 0.0     # all of it is tiny
+
+
+def test_traffic_lookup_follows_the_source_hash(tmp_path, monkeypatch):
+    src = tmp_path / "kernel.cu"
+    src.write_text("// one version\n")
+    h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    entry = {"workload": "w", "bytes_per_launch": 123.0, "source": "kernel.cu", "source_sha256_16": h}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"attn_long": [entry]}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic("attn_long", "w") == 123.0
+    assert bench.load_traffic("attn_long", "other") is None
+    assert bench.load_traffic("attn_tiny", "w") is None
+    src.write_text("// another version\n")                        # the kernel changed since the capture
+    assert bench.load_traffic("attn_long", "w") is None
+
+
+def test_committed_traffic_entries_name_existing_sources():
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        d = json.load(f)
+    for kernel, entries in d.items():
+        for e in entries:
+            assert os.path.exists(os.path.join(bench.ROOT, e["source"])), e
+            assert e["bytes_per_launch"] > 0
+
+
+def test_peaks_fall_back_when_the_measured_file_is_absent(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    peaks, src = bench.load_peaks()
+    assert peaks["hbm_gbs"] > 0 and peaks["bf16_tflops_sustained"] > 0
+    assert "fallback" in src
