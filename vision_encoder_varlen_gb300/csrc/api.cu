@@ -54,9 +54,9 @@ vit_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? VIT_OK : VIT_E
 
 constexpr int64_t kMaxTokens = (int64_t)1 << 31;
 
-// Segments longer than this run on the tcgen05 long-segment kernel.
-// Measured crossover on GB300: the warp-MMA kernel wins below ~32 tokens, the two tie at
-// 32-64, the tcgen05 kernel wins from 64 tokens up (30 % at 64-128, 3x beyond).
+// Segments longer than this run on the tcgen05 long-segment kernel, the others on the
+// warp-MMA kernels. Measured on GB300: up to 64 tokens the tiny-segment kernel is 2-4x
+// faster than the tcgen05 kernel, from 64 tokens up the tcgen05 kernel wins.
 std::atomic<int> g_short_max{64};
 // Test hook: when set, the long-segment kernel never loads V, so its bounded waits expire.
 std::atomic<int> g_stall_v{0};

@@ -21,8 +21,10 @@
 //   - rows outside the segment are zero-filled on load and never read from
 //     HBM, so no other segment is ever touched; several CTAs per SM overlap
 //     one item's loads with another's arithmetic.
-// Any segment length works (longer ones loop over 128-key tiles); the
-// long-segment kernel normally takes those.
+// Any segment length works (longer ones loop over 128-key tiles). With the
+// default split it has no work: segments of at most 64 tokens go to the
+// tiny-segment kernel and longer ones to the tcgen05 kernel; it takes the band
+// between 64 tokens and a caller-raised split (vit_set_short_segment_max).
 #include "internal.h"
 #include "warp_mma.cuh"
 
