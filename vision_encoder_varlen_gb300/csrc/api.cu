@@ -237,6 +237,8 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
     sp.tiny_max = sp.short_max < attn_tiny_max() ? sp.short_max : attn_tiny_max();
     sp.bm_long = attn_long_bm();
     sp.bm_short = attn_short_bm();
+    // the scheduler divides by these with shifts
+    if ((sp.bm_long & (sp.bm_long - 1)) || (sp.bm_short & (sp.bm_short - 1))) return VIT_ERR_BAD_ARGUMENT;
     cudaError_t e = launch_schedule(padded ? nullptr : cu_seqlens, seq_start, seq_len, B, T, H, max_seqlen, sp, hdr,
                                     items, status_dev, s);
     if (e != cudaSuccess) return VIT_ERR_CUDA;

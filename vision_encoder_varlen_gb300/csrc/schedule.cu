@@ -160,13 +160,19 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
     __syncthreads();
 
     // ---- 3. item counts per position, exclusive scan, expansion
+    // (the block sizes are powers of two: shifts instead of divisions, which otherwise dominate
+    // this single block's instruction count for thousands of segments)
+    const int lg_long = __ffs(sp.bm_long) - 1, lg_short = __ffs(sp.bm_short) - 1;
+    auto n_blocks = [&](int len) {
+        const int lg = len > sp.short_max ? lg_long : lg_short;
+        return (len + (1 << lg) - 1) >> lg;
+    };
     int64_t local = 0, local_long = 0, local_tiny = 0;
     for (int p = lo; p < hi; ++p) {
         const int seg = s_order[p];
         const int len = s_len[seg];
         const bool is_long = len > sp.short_max;
-        const int bm = is_long ? sp.bm_long : sp.bm_short;
-        const int64_t n = (int64_t)H * ((len + bm - 1) / bm);
+        const int64_t n = (int64_t)H * n_blocks(len);
         local += n;
         if (is_long) local_long += n;
         else if (len <= sp.tiny_max) local_tiny += n;
@@ -176,11 +182,8 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
     block_exclusive_scan(local_long, s_warp, &total_long);
     block_exclusive_scan(local_tiny, s_warp, &total_tiny);
     for (int p = lo; p < hi; ++p) {
-        const int seg = s_order[p];
-        const int len = s_len[seg];
-        const int bm = len > sp.short_max ? sp.bm_long : sp.bm_short;
         s_off[p] = (int32_t)run;
-        run += (int64_t)H * ((len + bm - 1) / bm);
+        run += (int64_t)H * n_blocks(s_len[s_order[p]]);
     }
     __syncthreads();
     // one warp per sorted segment (a whole-block loop over B segments would leave most threads idle)
@@ -190,12 +193,16 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
         const int len = s_len[seg];
         if (len == 0) continue;
         const int bm = len > sp.short_max ? sp.bm_long : sp.bm_short;
-        const int nq = (len + bm - 1) / bm;
+        const int nq = n_blocks(len);
         const int start = s_start[seg];
         Item *dst = items + s_off[p];
-        for (int i = lane; i < H * nq; i += 32) {
-            const int h = i / nq, qb = i - h * nq;
-            dst[i] = make_int4(start, len, start + qb * bm, h);
+        if (nq == 1) {                                     // one query block: item i is head i
+            for (int i = lane; i < H; i += 32) dst[i] = make_int4(start, len, start, i);
+        } else {
+            for (int i = lane; i < H * nq; i += 32) {
+                const int h = i / nq, qb = i - h * nq;
+                dst[i] = make_int4(start, len, start + qb * bm, h);
+            }
         }
     }
     if (tid == 0) {
