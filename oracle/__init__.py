@@ -29,8 +29,17 @@ _i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
 _u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
 
 
+# A prebuilt oracle library to load instead of building vit_oracle.c: the mutation test
+# (tests/test_oracle_mutants.py) compiles deliberately broken copies of the source and runs
+# the pins against each through this variable.
+_OVERRIDE_ENV = "VIT_ORACLE_LIB_OVERRIDE"
+
+
 def build(force: bool = False) -> str:
     """Compile the C oracle with gcc (OpenMP if available). Returns the .so path."""
+    override = os.environ.get(_OVERRIDE_ENV)
+    if override:
+        return override
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
         return _LIB_PATH
