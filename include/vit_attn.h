@@ -18,7 +18,7 @@
  *   - All pointers named *_dev or documented "device" are CUDA device pointers
  *     on the current device. The caller owns every buffer; the library never
  *     allocates or frees device memory and keeps no device state between
- *     calls.
+ *     calls (apart from the fixed array behind vit_varlen_attn_noalloc).
  *   - Calls are asynchronous on `stream` (0 = legacy default stream) and never
  *     synchronise, except vit_read_status and vit_kernel_timing_read.
  *   - bf16 tensors are raw 16-bit bfloat16 values ("const void*"), row-major,
@@ -30,9 +30,12 @@
  *     longer than max_seqlen, a grid that does not sum to T, a wait that timed
  *     out) are written into *status_dev when status_dev is non-NULL: kernels
  *     only ever store a negative code there and the first error wins, so the
- *     caller zeroes the word once and reads it with vit_read_status. On a
- *     device-detected error the affected call computes nothing and leaves its
- *     outputs untouched. No kernel traps or waits without a bound.
+ *     caller zeroes the word once and reads it with vit_read_status. For
+ *     malformed offsets or lengths and a grid that does not sum to T, the
+ *     affected call computes nothing and leaves its outputs untouched; after
+ *     an expired wait (VIT_ERR_TIMEOUT) or a token position outside the rope
+ *     table (VIT_ERR_POSITION_RANGE) its outputs are undefined, but nothing is
+ *     read or written out of bounds. No kernel traps or waits without a bound.
  */
 #ifndef VIT_ATTN_H
 #define VIT_ATTN_H
