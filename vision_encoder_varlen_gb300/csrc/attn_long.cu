@@ -31,11 +31,14 @@
 //               region of TMEM, and the epilogue O / l -> bf16 -> HBM.
 // TMEM (512 columns): S0 | S1 | O0 | O1 | P0 | P1; the key tile BN is the
 // largest that fits (128 for head_dim <= 64, 112 for 80, 96 for 96, 80 for
-// 128), so the two tiles never wait for each other.  Keys past the segment end are
-// masked to -inf (they contribute exactly 0), query rows past it are never
-// stored, rows past T are zero-filled by TMA: no item reads or writes any
-// other segment's results. Every wait is bounded; a wait that expires sets
-// VIT_ERR_TIMEOUT, and all roles drain and free TMEM before exiting.
+// 128), so the two tiles never wait for each other. Keys past the segment end are
+// masked to -inf; the last tile of a segment that ends inside it runs only the
+// 16-key steps holding its keys, with the leftover V rows zeroed, so no value
+// outside the segment (finite or not) enters a result; query rows past it are
+// never stored, rows past T are zero-filled by TMA. Template switches add the
+// per-row log-sum-exp store (LSE) and the Q rotation in warp 3 (FQ) without
+// touching the plain kernel's code. Every wait is bounded; a wait that expires
+// sets VIT_ERR_TIMEOUT, and all roles drain and free TMEM before exiting.
 #include <cudaTypedefs.h>
 
 #include <type_traits>
