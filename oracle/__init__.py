@@ -5,7 +5,9 @@ leg may import this package. The CUDA library never loads it and shares no
 code with it. The arithmetic lives in ``vit_oracle.c`` (form B: one plain
 softmax attention per packed segment, after RMSNorm and 2D RoPE) and in
 ``dense_ref.py`` (form A: one dense attention with a block-diagonal additive
-mask); see those files for the passages each step follows.
+mask); see those files for the passages each step follows. ``mimic.py`` repeats
+the steps with the roundings of the pages' eager modules; it explains residuals
+and never decides a pass or a failure.
 """
 from __future__ import annotations
 
