@@ -86,6 +86,10 @@ def test_host_validation_without_gpu(L):
     assert _attn(L, scale=float("nan")) == -14
     assert _attn(L, cu=0, B=3) == -14               # uniform split needs T % B == 0
     assert _attn(L, T=0, B=0) == 0                  # nothing to do
+    # token indices are int32 (cu_seqlens, positions, work items): T must stay below 2^31,
+    # including for the uniform split, whose segment starts the scheduler derives from T
+    assert _attn(L, T=1 << 31, max_seqlen=1 << 30) == -3
+    assert _attn(L, T=1 << 31, cu=0, B=2, max_seqlen=1 << 30) == -3
 
 
 def test_prologue_and_rope_validation_without_gpu(L):
@@ -105,6 +109,9 @@ def test_prologue_and_rope_validation_without_gpu(L):
     assert L.vit_rope_freqs(40, 10000.0, None, 1, 4, p(16), p(16), p(16), None, None) == -1
     assert L.vit_rope_freqs(40, 10000.0, p(16), 9000, 4, p(16), p(16), p(16), None, None) == -7
     assert L.vit_rope_freqs(40, 10000.0, p(16), 1, 4, None, None, None, None, None) == 0
+    assert L.vit_rope_freqs(40, 10000.0, p(16), 1, 1 << 31, p(16), p(16), p(16), None, None) == -3
+    assert L.vit_qk_norm_rope(p(16), p(16), p(16), p(16), 1 << 31, 2, 80, 160, 160, 160, 160, p(16), p(16),
+                              None, 1e-6, None) == -3
 
 
 def test_extended_calls_validation_without_gpu(L):
