@@ -87,6 +87,7 @@ class ClockSampler:
         self.path = None
 
     def __enter__(self):
+        self.f = None
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
@@ -95,8 +96,13 @@ class ClockSampler:
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
-        except Exception:
+        except Exception:             # no nvidia-smi: the line reports clocks as null
             self.proc = None
+            if self.f is not None:
+                self.f.close()
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+            self.path = None
         return self
 
     def __exit__(self, *exc):

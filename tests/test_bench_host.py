@@ -54,3 +54,24 @@ def test_peaks_fall_back_when_the_measured_file_is_absent(tmp_path, monkeypatch)
     peaks, src = bench.load_peaks()
     assert peaks["hbm_gbs"] > 0 and peaks["bf16_tflops_sustained"] > 0
     assert "fallback" in src
+
+
+def test_clock_sampler_summary_and_missing_tool(tmp_path, monkeypatch):
+    # the summary of a sampled CSV: median SM clock under load, the max, the active reasons
+    s = bench.ClockSampler(0)
+    path = tmp_path / "clocks.csv"
+    rows = ["0, 2032, 2070, 1100.5, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 2040, 2070, 1150.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 345, 2070, 90.0, 0x1, Not Active, Not Active, Not Active, Not Active",   # idle sample
+            "0, 2010, 2070, 1200.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "garbage line"]
+    path.write_text("\n".join(rows) + "\n")
+    s.proc, s.path = object(), str(path)
+    got = s.summary()
+    assert got == {"sm_mhz": 2032.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 4}
+    assert not path.exists()                               # the temporary file is removed
+    # without nvidia-smi the sampler reports nothing and leaves no file behind
+    monkeypatch.setattr(bench.subprocess, "Popen", lambda *a, **k: (_ for _ in ()).throw(FileNotFoundError()))
+    with bench.ClockSampler(0) as c:
+        pass
+    assert c.summary() is None and c.path is None
