@@ -46,26 +46,34 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def compile_flags(ptxas_info: bool = False) -> list:
+    flags = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+    return flags + (["-Xptxas", "-v"] if ptxas_info else [])
+
+
+def compile_all(out_dir: str, ptxas_info: bool = False) -> list:
+    """Compile every translation unit into out_dir in parallel; [(object path, compiler stderr)]."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
-    common = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
-    if ptxas_info:
-        common += ["-Xptxas", "-v"]
+    os.makedirs(out_dir, exist_ok=True)
+    flags = compile_flags(ptxas_info)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [nvcc, *common, "-c", src, "-o", obj]
-        r = subprocess.run(cmd, capture_output=True, text=True)
+        obj = os.path.join(out_dir, os.path.basename(src) + ".o")
+        r = subprocess.run([nvcc, *flags, "-c", src, "-o", obj], capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stderr}")
         return obj, r.stderr
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
-        results = list(ex.map(compile_one, _sources()))
+        return list(ex.map(compile_one, _sources()))
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+    if not force and up_to_date():
+        return LIB
+    nvcc = _nvcc()
+    os.makedirs(LIBDIR, exist_ok=True)
+    results = compile_all(BUILD, ptxas_info)
     for obj, err in results:
         if verbose and err.strip():
             print(err, file=sys.stderr)
