@@ -222,7 +222,11 @@ size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D);
  *   B             number of segments, 1 <= B <= VIT_MAX_SEGMENTS.
  *   max_seqlen    an upper bound on the segment lengths (may be padded to a
  *                 CUDA-graph bucket, [TS] round_up_to_bucket); a segment longer
- *                 than it is a device error. Used for validation only.
+ *                 than it is a device error. 0 = not given: T is taken as the
+ *                 bound (where [TS] _varlen_metadata reads the exact maximum back
+ *                 to the host, this needs no synchronisation). Used for
+ *                 validation and to skip the long-segment kernel when no segment
+ *                 can be long; never for the results. Negative: VIT_ERR_BAD_ARGUMENT.
  *   scale         softmax scale; <= 0 selects 1/sqrt(D) ([TS] head_size**-0.5).
  *   out           device bf16 [T, H, D] with token stride out_stride (the
  *                 [T, H*D] layout the output projection takes).
@@ -310,7 +314,8 @@ vit_status_t vit_varlen_attn_fused_q(const void *q, const void *k, const void *v
  *   seq_start   device int32 [B]: first row of each segment, ascending.
  *   seq_len     device int32 [B]: real length of each segment (0 allowed).
  *               Checked on the device: every segment inside [0, T), after the
- *               previous segment's end, and no longer than max_seqlen;
+ *               previous segment's end, and no longer than max_seqlen (0:
+ *               not given, T is the bound, as in vit_varlen_attn);
  *               otherwise VIT_ERR_BAD_SEQLENS / VIT_ERR_SEQLEN_EXCEEDS_MAX and
  *               nothing is computed.
  *   B           0 <= B <= VIT_MAX_SEGMENTS (0: nothing to do).

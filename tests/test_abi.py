@@ -82,7 +82,7 @@ def test_host_validation_without_gpu(L):
     assert _attn(L, ws=0) == -1
     assert _attn(L, ws=264) == -5                   # workspace misaligned
     assert _attn(L, ws_bytes=64) == -6
-    assert _attn(L, max_seqlen=0) == -14
+    assert _attn(L, max_seqlen=-1) == -14            # 0 means "not given" (T bounds it); negative is an error
     assert _attn(L, scale=float("nan")) == -14
     assert _attn(L, cu=0, B=3) == -14               # uniform split needs T % B == 0
     assert _attn(L, T=0, B=0) == 0                  # nothing to do

@@ -88,6 +88,23 @@ def test_uniform_segments_without_cu_seqlens(split):
     assert_close(out, ref, what="uniform")
 
 
+def test_max_seqlen_not_given(split):
+    # None (0 in the C ABI): T bounds the segments; the work items and so the results are those
+    # of a call given the exact maximum, bit for bit, for packed, uniform and padded layouts
+    lengths = [1, 300, 0, 64, 65, 129]
+    w, t, cu, (q, k, v) = _inputs(lengths, 2, 80, seed=9)
+    bits = lambda x: x.view(torch.int16)                 # noqa: E731
+    status = vit.new_status()
+    got = vit.varlen_attn(q, k, v, cu, None, status=status)
+    assert vit.read_status(status) == 0
+    assert torch.equal(bits(got), bits(vit.varlen_attn(q, k, v, cu, 300)))
+    q4, k4, v4 = q[:120], k[:120], v[:120]
+    assert torch.equal(bits(vit.varlen_attn(q4, k4, v4, None, None, num_segments=4)),
+                       bits(vit.varlen_attn(q4, k4, v4, None, 30, num_segments=4)))
+    start, length = cu[:-1].contiguous(), (cu[1:] - cu[:-1]).contiguous()
+    assert torch.equal(bits(vit.varlen_attn_padded(q, k, v, start, length, None)), bits(got))
+
+
 def test_in_place_prologue_matches_out_of_place():
     w = wl.make_config(3)
     t = w.tensors()

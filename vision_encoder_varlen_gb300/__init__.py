@@ -203,15 +203,22 @@ def workspace_size(T: int, H: int, B: int, D: int) -> int:
     return int(lib().vit_varlen_attn_workspace_size(int(T), int(H), int(B), int(D)))
 
 
+def _max_seqlen(m) -> int:
+    """The C convention: 0 = not given (the library bounds the segments by T)."""
+    return 0 if m is None else int(m)
+
+
 def varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor | None,
-                max_seqlen: int, scale: float | None = None, *, num_segments: int | None = None,
+                max_seqlen: int | None = None, scale: float | None = None, *, num_segments: int | None = None,
                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                 status: torch.Tensor | None = None, return_lse: bool = False, lse: torch.Tensor | None = None,
                 stream=None):
     """Non-causal attention inside each packed segment. q, k, v [T, H, D] bf16 -> out [T, H, D] bf16.
 
-    With ``return_lse`` (or an ``lse`` buffer) also returns lse [T, H] fp32, the natural-log
-    sum of exp(scale * q.k) over each row's segment: (out, lse)."""
+    ``max_seqlen`` bounds the segment lengths (a padded bucket is fine); None leaves the bound
+    to the library (T), so nothing is read back to the host. With ``return_lse`` (or an ``lse``
+    buffer) also returns lse [T, H] fp32, the natural-log sum of exp(scale * q.k) over each
+    row's segment: (out, lse)."""
     T, H, D = q.shape
     qs, ks, vs = _tok_stride(q, "q", H, D), _tok_stride(k, "k", H, D), _tok_stride(v, "v", H, D)
     if cu_seqlens is not None:
@@ -232,21 +239,21 @@ def varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: t
     ws_bytes = workspace.numel() * workspace.element_size()
     if not return_lse and lse is None:
         _check(lib().vit_varlen_attn(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, _ptr(cu_seqlens), B,
-                                     int(max_seqlen), sc, _ptr(out), os_, _ptr(workspace), ws_bytes, _ptr(status),
-                                     _stream(stream)), "vit_varlen_attn")
+                                     _max_seqlen(max_seqlen), sc, _ptr(out), os_, _ptr(workspace), ws_bytes,
+                                     _ptr(status), _stream(stream)), "vit_varlen_attn")
         return out
     if lse is None:
         lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (T, H) or not lse.is_contiguous() or not lse.is_cuda:
         raise ValueError(f"lse must be a contiguous CUDA float32 tensor [{T}, {H}]")
     _check(lib().vit_varlen_attn_lse(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, _ptr(cu_seqlens), B,
-                                     int(max_seqlen), sc, _ptr(out), os_, _ptr(lse), _ptr(workspace), ws_bytes,
+                                     _max_seqlen(max_seqlen), sc, _ptr(out), os_, _ptr(lse), _ptr(workspace), ws_bytes,
                                      _ptr(status), _stream(stream)), "vit_varlen_attn_lse")
     return out, lse
 
 
 def varlen_attn_fused_q(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor | None,
-                        max_seqlen: int, pos_hw: torch.Tensor, cos_sin: torch.Tensor,
+                        max_seqlen: int | None, pos_hw: torch.Tensor, cos_sin: torch.Tensor,
                         q_norm_w: torch.Tensor | None = None, eps: float = 1e-6, scale: float | None = None, *,
                         interleaved: bool = False, num_segments: int | None = None,
                         out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
@@ -283,7 +290,7 @@ def varlen_attn_fused_q(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_se
                 q_norm_w.data_ptr() if q_norm_w is not None else None, float(eps),
                 ROPE_INTERLEAVED if interleaved else ROPE_ROTATE_HALF)
     _check(lib().vit_varlen_attn_fused_q(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, ctypes.byref(qr),
-                                         _ptr(cu_seqlens), B, int(max_seqlen),
+                                         _ptr(cu_seqlens), B, _max_seqlen(max_seqlen),
                                          float(scale) if scale is not None else 0.0, _ptr(out), os_, _ptr(lse),
                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
                                          _ptr(status), _stream(stream)), "vit_varlen_attn_fused_q")
@@ -291,7 +298,7 @@ def varlen_attn_fused_q(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_se
 
 
 def varlen_attn_padded(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_start: torch.Tensor,
-                       seq_len: torch.Tensor, max_seqlen: int, scale: float | None = None, *,
+                       seq_len: torch.Tensor, max_seqlen: int | None = None, scale: float | None = None, *,
                        out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                        status: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
     """Attention over a padded layout: segment i is rows [seq_start[i], seq_start[i] + seq_len[i]) of
@@ -314,14 +321,16 @@ def varlen_attn_padded(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_st
     if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (T, H) or not lse.is_contiguous()):
         raise ValueError(f"lse must be a contiguous CUDA float32 tensor [{T}, {H}]")
     _check(lib().vit_varlen_attn_padded(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, _ptr(seq_start),
-                                        _ptr(seq_len), B, int(max_seqlen), float(scale) if scale is not None else 0.0,
-                                        _ptr(out), os_, _ptr(lse), None, _ptr(workspace),
+                                        _ptr(seq_len), B, _max_seqlen(max_seqlen),
+                                        float(scale) if scale is not None else 0.0, _ptr(out), os_, _ptr(lse), None,
+                                        _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
            "vit_varlen_attn_padded")
     return out
 
 
-def encoder_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen: int,
+def encoder_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                 max_seqlen: int | None,
                  pos_hw: torch.Tensor, inv_freq: torch.Tensor, cos_sin: torch.Tensor,
                  norm_w: torch.Tensor | None = None, eps: float = 1e-6, *, interleaved: bool = False,
                  k_out: torch.Tensor | None = None, **kw):

@@ -193,7 +193,11 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
     if (T < 0 || T >= kMaxTokens || H < 1 || B < 0) return VIT_ERR_BAD_SHAPE;
     if (B > VIT_MAX_SEGMENTS) return VIT_ERR_TOO_MANY_SEGMENTS;
     if (B == 0) return T == 0 ? VIT_OK : VIT_ERR_BAD_SHAPE;
-    if (max_seqlen < 0 || (T > 0 && max_seqlen < 1)) return VIT_ERR_BAD_ARGUMENT;
+    if (max_seqlen < 0) return VIT_ERR_BAD_ARGUMENT;
+    // 0 = not given: every segment lies inside [0, T), so T bounds it. ([TS] _varlen_metadata
+    // derives the exact maximum with a device-to-host read instead; a bound is all that is
+    // needed here, and taking T keeps the call free of host synchronisation.)
+    if (max_seqlen == 0) max_seqlen = (int)T;
     if (isnan(scale) || isinf(scale)) return VIT_ERR_BAD_ARGUMENT;
     if (padded) {
         if (!seq_start) return VIT_ERR_NULL_POINTER;
