@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "trace.h"
 
 namespace vit {
 size_t schedule_smem_bytes(int B);
@@ -102,6 +103,7 @@ vit_status_t vit_device_supported(int device)
 vit_status_t vit_rope_freqs(int dim, float theta, const int32_t *grid_hw, int n_img, int64_t T, float *inv_freq,
                             int32_t *pos_hw, int32_t *cu_seqlens, int32_t *status_dev, vit_stream_t stream)
 {
+    TraceRange trace("vit_rope_freqs");
     if (dim < 2 || dim % 2 != 0 || dim > 256) return VIT_ERR_BAD_ARGUMENT;
     if (!(theta > 0.f) || !isfinite(theta)) return VIT_ERR_BAD_ARGUMENT;
     if (n_img < 0 || T < 0 || T >= kMaxTokens) return VIT_ERR_BAD_SHAPE;
@@ -115,11 +117,11 @@ vit_status_t vit_rope_freqs(int dim, float theta, const int32_t *grid_hw, int n_
                                        (cudaStream_t)stream));
 }
 
-vit_status_t vit_qk_norm_rope_ex(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T, int H,
-                                 int D, int64_t q_in_stride, int64_t q_out_stride, int64_t k_in_stride,
-                                 int64_t k_out_stride, const int32_t *pos_hw, const float *inv_freq,
-                                 const void *norm_w, float eps, int rope_mode, int32_t *status_dev,
-                                 vit_stream_t stream)
+static vit_status_t qk_norm_rope_impl(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T,
+                                      int H, int D, int64_t q_in_stride, int64_t q_out_stride, int64_t k_in_stride,
+                                      int64_t k_out_stride, const int32_t *pos_hw, const float *inv_freq,
+                                      const void *norm_w, float eps, int rope_mode, int32_t *status_dev,
+                                      vit_stream_t stream)
 {
     if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
     if (T < 0 || T >= kMaxTokens || H < 1) return VIT_ERR_BAD_SHAPE;
@@ -148,17 +150,30 @@ vit_status_t vit_qk_norm_rope_ex(const void *q_in, void *q_out, const void *k_in
                                          rope_mode == VIT_ROPE_INTERLEAVED, sms, status_dev, (cudaStream_t)stream));
 }
 
+vit_status_t vit_qk_norm_rope_ex(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T, int H,
+                                 int D, int64_t q_in_stride, int64_t q_out_stride, int64_t k_in_stride,
+                                 int64_t k_out_stride, const int32_t *pos_hw, const float *inv_freq,
+                                 const void *norm_w, float eps, int rope_mode, int32_t *status_dev,
+                                 vit_stream_t stream)
+{
+    TraceRange trace("vit_qk_norm_rope_ex");
+    return qk_norm_rope_impl(q_in, q_out, k_in, k_out, T, H, D, q_in_stride, q_out_stride, k_in_stride, k_out_stride,
+                             pos_hw, inv_freq, norm_w, eps, rope_mode, status_dev, stream);
+}
+
 vit_status_t vit_qk_norm_rope(const void *q_in, void *q_out, const void *k_in, void *k_out, int64_t T, int H, int D,
                               int64_t q_in_stride, int64_t q_out_stride, int64_t k_in_stride, int64_t k_out_stride,
                               const int32_t *pos_hw, const float *inv_freq, const void *norm_w, float eps,
                               vit_stream_t stream)
 {
-    return vit_qk_norm_rope_ex(q_in, q_out, k_in, k_out, T, H, D, q_in_stride, q_out_stride, k_in_stride,
-                               k_out_stride, pos_hw, inv_freq, norm_w, eps, VIT_ROPE_ROTATE_HALF, nullptr, stream);
+    TraceRange trace("vit_qk_norm_rope");
+    return qk_norm_rope_impl(q_in, q_out, k_in, k_out, T, H, D, q_in_stride, q_out_stride, k_in_stride, k_out_stride,
+                             pos_hw, inv_freq, norm_w, eps, VIT_ROPE_ROTATE_HALF, nullptr, stream);
 }
 
 vit_status_t vit_rope_table(const float *inv_freq, int head_dim, int max_pos, float *cos_sin, vit_stream_t stream)
 {
+    TraceRange trace("vit_rope_table");
     if (!head_dim_ok(head_dim)) return VIT_ERR_BAD_HEAD_DIM;
     if (max_pos < 1) return VIT_ERR_BAD_ARGUMENT;
     if (!inv_freq || !cos_sin) return VIT_ERR_NULL_POINTER;
@@ -300,6 +315,7 @@ vit_status_t vit_varlen_attn_lse(const void *q, const void *k, const void *v, in
                                  int B, int max_seqlen, float scale, void *out, int64_t out_stride, float *lse,
                                  void *workspace, size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
 {
+    TraceRange trace("vit_varlen_attn_lse");
     return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, nullptr, cu_seqlens, nullptr, nullptr, B,
                             max_seqlen, scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
 }
@@ -310,6 +326,7 @@ vit_status_t vit_varlen_attn_fused_q(const void *q, const void *k, const void *v
                                      float scale, void *out, int64_t out_stride, float *lse, void *workspace,
                                      size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
 {
+    TraceRange trace("vit_varlen_attn_fused_q");
     if (!q_rope) return VIT_ERR_NULL_POINTER;
     return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, q_rope, cu_seqlens, nullptr, nullptr, B,
                             max_seqlen, scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
@@ -321,6 +338,7 @@ vit_status_t vit_varlen_attn_padded(const void *q, const void *k, const void *v,
                                     int64_t out_stride, float *lse, const vit_q_rope_t *q_rope, void *workspace,
                                     size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
 {
+    TraceRange trace("vit_varlen_attn_padded");
     if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
     if (T < 0 || T >= kMaxTokens || H < 1 || B < 0) return VIT_ERR_BAD_SHAPE;
     if (B == 0) return VIT_OK;                           // every row is padding: nothing to compute
@@ -334,8 +352,9 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
                              float scale, void *out, int64_t out_stride, void *workspace, size_t workspace_bytes,
                              int32_t *status_dev, vit_stream_t stream)
 {
-    return vit_varlen_attn_lse(q, k, v, T, H, D, q_stride, k_stride, v_stride, cu_seqlens, B, max_seqlen, scale, out,
-                               out_stride, nullptr, workspace, workspace_bytes, status_dev, stream);
+    TraceRange trace("vit_varlen_attn");
+    return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, nullptr, cu_seqlens, nullptr, nullptr, B,
+                            max_seqlen, scale, out, out_stride, nullptr, workspace, workspace_bytes, status_dev, stream);
 }
 
 int vit_debug_stall_long_kernel(int enable)
@@ -350,6 +369,7 @@ int vit_set_short_segment_max(int short_max)
 
 vit_status_t vit_read_status(const int32_t *status_dev, vit_stream_t stream)
 {
+    TraceRange trace("vit_read_status");
     if (!status_dev) return VIT_ERR_NULL_POINTER;
     int32_t h = 0;
     cudaStream_t s = (cudaStream_t)stream;

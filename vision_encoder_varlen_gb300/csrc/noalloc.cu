@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "trace.h"
 
 namespace {
 
@@ -46,6 +47,7 @@ extern "C" vit_status_t vit_varlen_attn_noalloc(const void *q, const void *k, co
                                                 void *out, int64_t out_stride, int32_t *status_dev,
                                                 vit_stream_t stream)
 {
+    vit::TraceRange trace("vit_varlen_attn_noalloc");
     // sizes whose work list does not fit the fixed array are refused before anything runs
     const size_t need = vit_varlen_attn_workspace_size(T, H, B, D);
     if (need > (size_t)VIT_NOALLOC_WORKSPACE_BYTES) return VIT_ERR_WORKSPACE_TOO_SMALL;
