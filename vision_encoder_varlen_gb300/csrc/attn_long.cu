@@ -66,7 +66,8 @@ template <int D> struct LongCfg {
     // K/V ring of 3 slots; the next item's Q pair is prefetched into a second Q buffer
     // where that still fits in shared memory (all head dims but 128)
     static constexpr int STAGES = 3;
-    static constexpr int QBUF = (4 * (D / 16) * BM * 32 + 3 * 2 * (D / 16) * BN * 32 + 1024 <= 231 * 1024) ? 2 : 1;
+    static constexpr int QBUF =
+        (4 * (D / 16) * BM * 32 + STAGES * 2 * (D / 16) * BN * 32 + 1024 <= 227 * 1024) ? 2 : 1;
     static constexpr int NSLAB = D / 16;
     static constexpr int Q_SLAB = BM * 32;                 // bytes of one 16-column slab of a Q tile
     static constexpr int KV_SLAB = BN * 32;
@@ -84,6 +85,7 @@ template <int D> struct LongCfg {
     static constexpr int TS0 = 0, TS1 = BN, TO0 = 2 * BN, TO1 = 2 * BN + D, TP0 = 2 * BN + 2 * D;
     static constexpr int TP1 = (TP0 + BN / 2 + 7) / 8 * 8;
     static_assert(TP1 + BN / 2 <= 512, "TMEM budget");
+    static_assert(SMEM <= 227 * 1024, "shared memory per block (227 KB opt-in limit)");
     static_assert(D % 16 == 0 && BN % 16 == 0 && (BN / 2) % 8 == 0, "tile shapes");
 };
 
