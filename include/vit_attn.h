@@ -36,6 +36,9 @@
  *     an expired wait (VIT_ERR_TIMEOUT) or a token position outside the rope
  *     table (VIT_ERR_POSITION_RANGE) its outputs are undefined, but nothing is
  *     read or written out of bounds. No kernel traps or waits without a bound.
+ *   - Every call that launches or synchronises opens an NVTX range named after
+ *     itself in the "vitattn" domain and closes it on every return, so a
+ *     profiler shows each kernel launch under the call that made it.
  */
 #ifndef VIT_ATTN_H
 #define VIT_ATTN_H
