@@ -123,8 +123,8 @@ def main() -> None:
         gpu = (fmt(r["gpu_vs_exact"]), fmt(r["gpu_vs_mimic"]),
                f"{100 * r['prologue_same_bits']:.3f} %, {r['prologue_max_units']:.2f}") if "gpu_vs_exact" in r \
             else ("-", "-", "-")
-        print(f"| {r['workload']} | {r['rows']} | {fmt(r['mimic_vs_exact'])} | {gpu[0]} | {gpu[1]} | {gpu[2]} | {r['seconds']} |",
-              flush=True)
+        cells = [r["workload"], r["rows"], fmt(r["mimic_vs_exact"]), *gpu, r["seconds"]]
+        print("| " + " | ".join(str(c) for c in cells) + " |", flush=True)
 
 
 if __name__ == "__main__":
