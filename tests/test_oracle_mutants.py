@@ -27,7 +27,14 @@ MUTANTS = [
     ("lse without the max", "lse[r * H + h] = mx + log(sum);", "lse[r * H + h] = log(sum);"),
     ("positions transposed", "pos[2 * t] = r;", "pos[2 * t] = c;"),
     ("norm weight ignored", "xh[d] * inv_rms * (w ? bf16_to_f64(w[d]) : 1.0)", "xh[d] * inv_rms"),
+    ("values from the stream start", "const double *vr = v + ((lo + j) * H + h) * (int64_t)D;",
+     "const double *vr = v + (j * H + h) * (int64_t)D;"),
+    ("keys of head 0 only", "const double *kr = k + ((lo + j) * H + h) * (int64_t)D;",
+     "const double *kr = k + ((lo + j) * H) * (int64_t)D;"),
 ]
+
+# the pins run against each build: the hand-derived and library pins, and the property pins
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_properties.py"]
 
 
 def _build(src_text, out_dir, name):
@@ -42,7 +49,7 @@ def _build(src_text, out_dir, name):
 
 def _pins_pass(lib_path):
     env = dict(os.environ, VIT_ORACLE_LIB_OVERRIDE=lib_path)
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"), "-x",
+    r = subprocess.run([sys.executable, "-m", "pytest", *[os.path.join(ROOT, "tests", f) for f in PIN_FILES], "-x",
                         "-q", "-p", "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True, text=True)
     return r.returncode == 0, r.stdout[-400:]
 
