@@ -144,9 +144,9 @@ class Path:
     """Device-resident buffers and the three calls of one step."""
 
     def __init__(self, vit, w: wl.Workload, t: dict, device, lse: bool = False, interleaved: bool = False,
-                 fused_q: bool = False):
+                 fused_q: bool = False, short_max: int | None = None):
         self.vit, self.w = vit, w
-        self.interleaved, self.fused_q = interleaved, fused_q
+        self.interleaved, self.fused_q, self.short_max = interleaved, fused_q, short_max
         self.max_pos = int(w.grid_hw.max())
         T, H, D, B = w.total_tokens, w.heads, w.head_dim, w.num_segments
         self.grid = torch.from_numpy(w.grid_hw.copy()).to(device)
@@ -167,12 +167,12 @@ class Path:
             cs = vit.rope_table(inv_freq, w.head_dim, self.max_pos)
             vit.encoder_attn(self.q, self.k, self.v, cu, w.max_seqlen, pos, inv_freq, cs, self.nw, w.eps,
                              interleaved=self.interleaved, k_out=self.kr, out=self.out, workspace=self.ws,
-                             status=self.status, lse=self.lse)
+                             status=self.status, lse=self.lse, short_max=self.short_max)
             return
         vit.qk_norm_rope(self.q, self.k, pos, inv_freq, self.nw, w.eps, q_out=self.qr, k_out=self.kr,
                          interleaved=self.interleaved)
         vit.varlen_attn(self.qr, self.kr, self.v, cu, w.max_seqlen, out=self.out, workspace=self.ws,
-                        status=self.status, lse=self.lse)
+                        status=self.status, lse=self.lse, short_max=self.short_max)
 
 
 class E2EPipeline:
@@ -303,6 +303,153 @@ def cpu_baseline_sample(w: wl.Workload, t: dict, target_s: float):
             "seconds": wall, "useful_flops": flops}
 
 
+SUSTAINED_AFTER_S = 2.0      # a timed region at least this long is judged against the sustained peak
+
+
+def working_set_bytes(w: wl.Workload) -> int:
+    """q, k, v, q', k', out of one step."""
+    return 6 * w.total_tokens * w.heads * w.head_dim * 2
+
+
+def needs_flush(w: wl.Workload) -> bool:
+    return working_set_bytes(w) < 2 * L2_BYTES
+
+
+def config_dict(w: wl.Workload, args, world: int) -> dict:
+    """The workload a line measures; the same dict for both arms."""
+    ws = working_set_bytes(w)
+    return {"workload": w.name, "tokens": w.total_tokens, "segments": w.num_segments, "heads": w.heads,
+            "head_dim": w.head_dim, "qk_norm": w.qk_norm, "max_seqlen": w.max_seqlen,
+            "useful_flops_per_step": w.useful_flops,
+            "rope": "interleaved" if args.interleaved else "rotate_half", "lse": bool(args.lse),
+            "q_prologue": "fused into the attention Q load" if args.fused_q else "separate pass",
+            "l2": "L2 flushed between steps" if needs_flush(w) else
+            f"inputs larger than L2 ({ws / 2 ** 20:.0f} MiB working set)",
+            "parallelism": f"data-parallel over {world} ranks, one batch each, no exchange" if world > 1
+            else "single"}
+
+
+def time_steps(step, steps: int, stream, flush_buf) -> float:
+    """Total device ms of `steps` calls of step(): back to back when flush_buf is None, else
+    each step alone after a write of flush_buf (larger than L2), events around the step only."""
+    if flush_buf is None:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1)
+    total = 0.0
+    for _ in range(steps):
+        flush_buf.zero_()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        total += ev0.elapsed_time(ev1)
+    return total
+
+
+def roofline_entry(vit, w: wl.Workload, kt: dict, short_max: int, peaks: dict, peaks_src: str, timed_s: float,
+                   fused_q: bool):
+    """The dominant kernel's achieved rate: its algorithmic work per launch over its mean
+    event-timed launch duration, against the measured peak of its bound. A contraction takes the
+    burst bf16 peak unless its timed region ran SUSTAINED_AFTER_S or longer."""
+    if not kt:
+        return None
+    dom = max(kt.items(), key=lambda kv: kv[1][1])[0]
+    n, tot = kt[dom]
+    avg_s = tot / n * 1e-3
+    T, H, D = w.total_tokens, w.heads, w.head_dim
+    if dom == "attn_long":
+        alg = kernel_algorithmic_flops(w, dom, short_max)
+        key = "bf16_tflops_sustained" if timed_s >= SUSTAINED_AFTER_S else "bf16_tflops"
+        peak = peaks[key]
+        achieved = alg / avg_s / 1e12
+        return {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": load_traffic(dom, w.name),
+                "peak_source": f"{peaks_src} {key} (timed region {timed_s:.2f} s)",
+                "algorithmic_flops_per_launch": alg, "avg_ms": tot / n}
+    tiny_max = min(short_max, 64)
+    L = w.lengths
+    if dom == "attn_tiny":           # q, k, v read and out written once per token it owns
+        alg = 8.0 * float(L[L <= tiny_max].sum()) * H * D
+    elif dom == "attn_short":
+        alg = 8.0 * float(L[(L > tiny_max) & (L <= short_max)].sum()) * H * D
+    elif dom == "qk_norm_rope":      # q and k (k alone with --fused-q) read and written once
+        alg = (4.0 if fused_q else 8.0) * T * H * D
+    else:
+        alg = 8.0 * T
+    achieved = alg / avg_s / 1e9
+    return {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(dom, w.name),
+            "peak_source": f"{peaks_src} hbm_gbs", "algorithmic_bytes_per_launch": alg, "avg_ms": tot / n}
+
+
+def measure_device(vit, path, w, steps: int, warmup: int, stream, device, flush_buf, barrier=lambda: None):
+    """Warm up, then time `steps` steps with every launch event-timed on its stream.
+    Returns (ms per step, {kernel: (launches, total ms)}, launches, clock summary)."""
+    for _ in range(warmup):
+        path.step()
+    torch.cuda.synchronize()
+    code = vit.read_status(path.status)
+    if code != 0:
+        raise RuntimeError(f"{w.name}: device status {code}: {vit.status_string(code)}")
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = vit.launch_count()
+    vit.kernel_timing_read()
+    with ClockSampler(device.index or 0) as clocks:
+        vit.kernel_timing(True)
+        try:
+            total_ms = time_steps(path.step, steps, stream, flush_buf if needs_flush(w) else None)
+        finally:
+            vit.kernel_timing(False)
+        kt = vit.kernel_timing_read()
+    torch.cuda.synchronize()
+    barrier()
+    return total_ms / steps, kt, vit.launch_count() - launches0, clocks.summary()
+
+
+def measure_graph(path, w, steps: int, stream, flush_buf) -> float:
+    """ms per step when the whole step is captured once in a CUDA graph and replayed (how a
+    serving loop that buckets its shapes runs it: no per-launch host cost)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        path.step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        path.step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ms = time_steps(g.replay, steps, stream, flush_buf if needs_flush(w) else None) / steps
+    del g
+    return ms
+
+
+def per_config_entry(vit, idx: int, args, rank: int, device, stream, flush_buf, peaks, peaks_src) -> dict:
+    """One of the smaller workloads, measured in the same run as the headline line."""
+    w = wl.make_config(idx)
+    path = Path(vit, w, rank_inputs(w, rank), device, lse=args.lse, interleaved=args.interleaved,
+                fused_q=args.fused_q, short_max=args.short_max)
+    ms, kt, launches, clk = measure_device(vit, path, w, args.steps, args.warmup, stream, device, flush_buf)
+    short_max = args.short_max if args.short_max is not None else vit.DEFAULT_SHORT_MAX
+    timed_s = ms * args.steps / 1e3
+    graph_ms = measure_graph(path, w, args.steps, stream, flush_buf)
+    return {"config": config_dict(w, args, 1), "ms_per_step": ms, "tflops": w.useful_flops / (ms * 1e-3) / 1e12,
+            "tokens_per_s": w.total_tokens / (ms * 1e-3), "graph_ms_per_step": graph_ms,
+            "graph_tflops": w.useful_flops / (graph_ms * 1e-3) / 1e12,
+            "kernels": {name: {"launches": n, "avg_ms": tot / max(n, 1)} for name, (n, tot) in kt.items()},
+            "gpu_launches": launches, "clocks": clk,
+            "roofline": roofline_entry(vit, w, kt, short_max, peaks, peaks_src, timed_s, args.fused_q)}
+
+
 def run_ours(args, rank, world, local):
     import vision_encoder_varlen_gb300 as vit
     from vision_encoder_varlen_gb300 import _build
@@ -312,61 +459,23 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    if args.short_max is not None:
-        vit.set_short_segment_max(args.short_max)
     w = wl.make_config(args.config)
     t = rank_inputs(w, rank)
     T, H, D = w.total_tokens, w.heads, w.head_dim
-    path = Path(vit, w, t, device, lse=args.lse, interleaved=args.interleaved, fused_q=args.fused_q)
+    path = Path(vit, w, t, device, lse=args.lse, interleaved=args.interleaved, fused_q=args.fused_q,
+                short_max=args.short_max)
     stream = torch.cuda.current_stream()
     tensor_bytes = T * H * D * 2
-    working_set = 6 * tensor_bytes
-    flush = working_set < 2 * L2_BYTES
-    flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device) if flush else None
+    flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
-    for _ in range(args.warmup):
-        path.step()
-    torch.cuda.synchronize()
-    code = vit.read_status(path.status)
-    if code != 0:
-        raise RuntimeError(f"device status {code}: {vit.status_string(code)}")
-
     # ---- timed region: K steps, per-kernel CUDA events recorded live on the launch stream
-    barrier()
-    torch.cuda.synchronize()
-    launches0 = vit.launch_count()
-    vit.kernel_timing_read()
-    with ClockSampler(local) as clocks:
-        vit.kernel_timing(True)
-        if not flush:
-            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            ev0.record(stream)
-            for _ in range(args.steps):
-                path.step()
-            ev1.record(stream)
-            torch.cuda.synchronize()
-            total_ms = ev0.elapsed_time(ev1)
-        else:
-            total_ms = 0.0
-            for _ in range(args.steps):
-                flush_buf.zero_()
-                ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                ev0.record(stream)
-                path.step()
-                ev1.record(stream)
-                torch.cuda.synchronize()
-                total_ms += ev0.elapsed_time(ev1)
-        vit.kernel_timing(False)
-        kt = vit.kernel_timing_read()
-    torch.cuda.synchronize()
-    barrier()
-    launches = vit.launch_count() - launches0
-    ms = reduce_max(total_ms / args.steps, device)
-    clk = clocks.summary()
+    local_ms, kt, launches, clk = measure_device(vit, path, w, args.steps, args.warmup, stream, device, flush_buf,
+                                                 barrier)
+    ms = reduce_max(local_ms, device)
 
     # ---- end to end through the public API from pinned host memory
     e2e = None
@@ -392,63 +501,35 @@ def run_ours(args, rank, world, local):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "overlap": "step i+1's upload and step i's download on two copy streams run during compute"}
 
+    # ---- the other workloads of the study, each measured alone in this run (one GPU only)
+    per_config = None
+    if world == 1 and args.config == 5 and not args.no_per_config:
+        peaks, peaks_src = load_peaks()
+        per_config = {str(i): per_config_entry(vit, i, args, rank, device, stream, flush_buf, peaks, peaks_src)
+                      for i in (1, 2, 3, 4)}
+
     if rank != 0:
         return
     peaks, peaks_src = load_peaks()
     flops = w.useful_flops
     value = job_tflops(flops, world, ms)
-    kernels = {name: {"launches": n, "avg_ms": tot / max(n, 1)} for name, (n, tot) in kt.items()}
-    dom = max(kt.items(), key=lambda kv: kv[1][1])[0] if kt else None
-    roofline = None
-    if dom is not None:
-        n, tot = kt[dom]
-        avg_s = tot / n * 1e-3
-        short_max = vit.set_short_segment_max(128)
-        vit.set_short_segment_max(short_max)
-        if dom == "attn_long":
-            alg = kernel_algorithmic_flops(w, dom, short_max)
-            peak = peaks["bf16_tflops_sustained"]
-            achieved = alg / avg_s / 1e12
-            roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                        "frac": achieved / peak, "traffic": load_traffic(dom, w.name),
-                        "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside a long step loop)",
-                        "algorithmic_flops_per_launch": alg}
-        else:
-            tiny_max = min(short_max, 64)
-            if dom == "attn_tiny":       # q, k, v read and out written once per token it owns
-                L = w.lengths
-                alg = 8.0 * float(L[L <= tiny_max].sum()) * H * D
-            elif dom == "attn_short":
-                L = w.lengths
-                alg = 8.0 * float(L[(L > tiny_max) & (L <= short_max)].sum()) * H * D
-            elif dom == "qk_norm_rope":  # q and k (k alone with --fused-q) read and written once
-                alg = (4.0 if args.fused_q else 8.0) * T * H * D
-            else:
-                alg = 8.0 * T
-            achieved = alg / avg_s / 1e9
-            roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                        "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(dom, w.name),
-                        "peak_source": f"{peaks_src} hbm_gbs", "algorithmic_bytes_per_launch": alg}
+    short_max = args.short_max if args.short_max is not None else vit.DEFAULT_SHORT_MAX
+    timed_s = ms * args.steps / 1e3
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "tokens": T, "segments": w.num_segments, "heads": H, "head_dim": D,
-                   "qk_norm": w.qk_norm, "max_seqlen": w.max_seqlen, "useful_flops_per_step": flops,
-                   "rope": "interleaved" if args.interleaved else "rotate_half", "lse": bool(args.lse),
-                   "q_prologue": "fused into the attention Q load" if args.fused_q else "separate pass",
-                   "l2": "L2 flushed between steps" if flush else
-                   f"inputs larger than L2 ({working_set / 2 ** 20:.0f} MiB working set)",
-                   "parallelism": f"data-parallel over {world} ranks, one batch each, no exchange" if world > 1
-                   else "single"},
+        "config": config_dict(w, args, world),
         "tokens_per_s": T * world / (ms * 1e-3),
         "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": launches,
-        "kernels": kernels,
-        "roofline": roofline,
+        "kernels": {name: {"launches": n, "avg_ms": tot / max(n, 1)} for name, (n, tot) in kt.items()},
+        "roofline": roofline_entry(vit, w, kt, short_max, peaks, peaks_src, timed_s, args.fused_q),
     }
+    if per_config is not None:
+        line["per_config"] = per_config
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(w, t, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -461,35 +542,30 @@ def run_split_sweep(args):
     from vision_encoder_varlen_gb300 import _build
     _build.build()
     rng = np.random.default_rng(0)
-    prev = vit.set_short_segment_max(64)
-    try:
-        for D in (80, 128):
-            for lo, hi in ((4, 16), (16, 32), (32, 64), (64, 128), (128, 256), (256, 512)):
-                lengths = rng.integers(lo, hi + 1, size=8192 if hi <= 32 else (4096 if hi <= 128 else 2048))
-                w = wl.from_lengths(lengths, 16, D, max_seqlen_meta=4096)
-                g = torch.Generator(device="cuda").manual_seed(1)
-                T = w.total_tokens
-                q, k, v = (torch.randn(T, 16, D, device="cuda", generator=g).to(torch.bfloat16) for _ in range(3))
-                cu = torch.from_numpy(w.cu_seqlens).cuda()
-                ws = torch.empty(vit.workspace_size(T, 16, w.num_segments, D), dtype=torch.uint8, device="cuda")
-                out = torch.empty_like(q)
-                res = {}
-                for name, sm in (("warp_mma_kernels_ms", 1 << 30), ("tcgen05_kernel_ms", 0)):
-                    vit.set_short_segment_max(sm)
-                    for _ in range(args.warmup):
-                        vit.varlen_attn(q, k, v, cu, 4096, out=out, workspace=ws)
-                    torch.cuda.synchronize()
-                    vit.kernel_timing_read()
-                    vit.kernel_timing(True)
-                    for _ in range(args.steps):
-                        vit.varlen_attn(q, k, v, cu, 4096, out=out, workspace=ws)
-                    vit.kernel_timing(False)
-                    kt = vit.kernel_timing_read()
-                    res[name] = sum(t for _, t in kt.values()) / args.steps
-                print(json.dumps({"sweep": "split", "head_dim": D, "lengths": [lo, hi], "segments": int(len(lengths)),
-                                  "tokens": T, **res}), flush=True)
-    finally:
-        vit.set_short_segment_max(prev)
+    for D in (80, 128):
+        for lo, hi in ((4, 16), (16, 32), (32, 64), (64, 128), (128, 256), (256, 512)):
+            lengths = rng.integers(lo, hi + 1, size=8192 if hi <= 32 else (4096 if hi <= 128 else 2048))
+            w = wl.from_lengths(lengths, 16, D, max_seqlen_meta=4096)
+            g = torch.Generator(device="cuda").manual_seed(1)
+            T = w.total_tokens
+            q, k, v = (torch.randn(T, 16, D, device="cuda", generator=g).to(torch.bfloat16) for _ in range(3))
+            cu = torch.from_numpy(w.cu_seqlens).cuda()
+            ws = torch.empty(vit.workspace_size(T, 16, w.num_segments, D), dtype=torch.uint8, device="cuda")
+            out = torch.empty_like(q)
+            res = {}
+            for name, sm in (("warp_mma_kernels_ms", 1 << 30), ("tcgen05_kernel_ms", 0)):
+                for _ in range(args.warmup):
+                    vit.varlen_attn(q, k, v, cu, 4096, out=out, workspace=ws, short_max=sm)
+                torch.cuda.synchronize()
+                vit.kernel_timing_read()
+                vit.kernel_timing(True)
+                for _ in range(args.steps):
+                    vit.varlen_attn(q, k, v, cu, 4096, out=out, workspace=ws, short_max=sm)
+                vit.kernel_timing(False)
+                kt = vit.kernel_timing_read()
+                res[name] = sum(t for _, t in kt.values()) / args.steps
+            print(json.dumps({"sweep": "split", "head_dim": D, "lengths": [lo, hi], "segments": int(len(lengths)),
+                              "tokens": T, **res}), flush=True)
 
 
 def run_reference(args, rank, world):
@@ -520,8 +596,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "tokens": w.total_tokens, "segments": w.num_segments, "heads": w.heads,
-                   "head_dim": w.head_dim, "qk_norm": w.qk_norm, "max_seqlen": w.max_seqlen},
+        "config": config_dict(w, args, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -541,6 +616,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload block (workloads 1-4 measured after the headline workload 5)")
     ap.add_argument("--sweep-split", action="store_true",
                     help="time both attention kernels over bands of segment lengths and exit")
     ap.add_argument("--short-max", type=int, default=None,

@@ -346,15 +346,21 @@ vit_status_t vit_varlen_attn_padded(const void *q, const void *k, const void *v,
  * Arguments, layouts and results are those of vit_varlen_attn without the
  * workspace pair: the scheduler's work list lives instead in a static device
  * array of VIT_NOALLOC_WORKSPACE_BYTES (4 MiB) inside this library, which
- * every GPU that loads the library keeps until the process exits. The call
- * itself allocates nothing (no cudaMalloc, no library allocator).
+ * every GPU that loads the library keeps while its CUDA context lives (until
+ * process exit, unless the context is reset). The call itself allocates
+ * nothing (no cudaMalloc, no cudaFree, no library allocator), and its output
+ * is bit-identical to vit_varlen_attn's on the same inputs.
  *   - Limit: sizes whose work list needs more than VIT_NOALLOC_WORKSPACE_BYTES
  *     (vit_varlen_attn_workspace_size(T, H, B, D) > 4 MiB; roughly
  *     H * (T/64 + B) > 262000 work items) return VIT_ERR_WORKSPACE_TOO_SMALL
  *     and launch nothing; use vit_varlen_attn with your own workspace there.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     Every other argument is checked first, exactly as vit_varlen_attn does.
+ *   - The first call in each CUDA context (the device's primary context, and
+ *     again after cudaDeviceReset or any other re-creation of it) looks up the
+ *     array's device address (cudaGetSymbolAddress, with that device current).
+ *     Make that call before any stream capture: a call that would need the
+ *     lookup while `stream` is being captured returns VIT_ERR_BAD_ARGUMENT and
+ *     touches nothing; later calls only launch.
  *   - All calls on a device share the one array, and it keeps whatever the
  *     previous call left there; every call rewrites what it reads, so nothing
  *     needs clearing, but two calls that overlap on the GPU (different streams
@@ -366,27 +372,43 @@ vit_status_t vit_varlen_attn_noalloc(const void *q, const void *k, const void *v
                                      void *out, int64_t out_stride, int32_t *status_dev, vit_stream_t stream);
 
 /*
- * Kernel split of vit_varlen_attn: segments longer than `short_max` tokens run
- * on the tcgen05/TMEM long-segment kernel (256 query rows per work item), the
- * others on warp-MMA kernels: segments of at most min(short_max, 64) tokens on
- * the tiny-segment kernel (one item per segment and head, the next item loaded
- * while the current one computes), longer ones on the short-segment kernel
- * (128 query rows per item). Default 64, the measured crossover on GB300.
- * 0 sends every segment to the long kernel, INT_MAX every segment to the short
- * one; the results agree within the output tolerance either way. Process-wide
- * setting read at each call; returns the previous value.
+ * Per-call options of vit_varlen_attn_ex. Every field has a "library default"
+ * value; a NULL options pointer means all defaults. The options only choose
+ * how the work is spread over the kernels: results agree within the output
+ * tolerance for every setting, and the workspace size does not depend on them.
+ *
+ *   short_segment_max   kernel split: segments longer than this many tokens run
+ *                       on the tcgen05/TMEM long-segment kernel, the others on
+ *                       warp-MMA kernels (segments of at most
+ *                       min(short_segment_max, 64) tokens on the tiny-segment
+ *                       kernel, one item per segment and head; longer ones on
+ *                       the short-segment kernel, 128 query rows per item).
+ *                       0 sends every segment to the long kernel, INT_MAX every
+ *                       segment to the warp-MMA kernels. -1 = library default
+ *                       (64, the measured crossover on GB300). Below -1:
+ *                       VIT_ERR_BAD_ARGUMENT.
  */
-int vit_set_short_segment_max(int short_max);
+typedef struct vit_attn_options {
+    int short_segment_max;
+} vit_attn_options_t;
 
 /*
- * Test hook for the failure path. While enabled (1), the long-segment kernel
- * skips its V tile loads, so the MMA warp's bounded wait expires: the call
- * stores VIT_ERR_TIMEOUT in status_dev, every warp gives up, the kernel frees
- * its tensor memory and exits, and the CUDA context stays usable. No fault,
- * trap or unbounded wait is involved. Outputs of such a call are undefined.
- * Returns the previous setting. Never enable it outside tests.
+ * The general attention call: every option of the calls above in one place.
+ * The segments come either from cu_seqlens (packed, as vit_varlen_attn; seq_start
+ * and seq_len NULL) or from seq_start and seq_len (a padded layout, as
+ * vit_varlen_attn_padded; cu_seqlens NULL); giving both is VIT_ERR_BAD_ARGUMENT.
+ * lse (vit_varlen_attn_lse) and q_rope (vit_varlen_attn_fused_q) may be NULL.
+ * opts: host pointer to per-call options, or NULL for the defaults. Nothing of
+ * a call's configuration is kept between calls, so threads that issue calls
+ * with different options do not affect one another.
  */
-int vit_debug_stall_long_kernel(int enable);
+vit_status_t vit_varlen_attn_ex(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                                const int32_t *cu_seqlens, const int32_t *seq_start, const int32_t *seq_len,
+                                int B, int max_seqlen, float scale,
+                                void *out, int64_t out_stride, float *lse, const vit_q_rope_t *q_rope,
+                                const vit_attn_options_t *opts, void *workspace, size_t workspace_bytes,
+                                int32_t *status_dev, vit_stream_t stream);
 
 /*
  * Synchronise `stream`, then read the status word. Returns VIT_OK, the first

@@ -39,6 +39,37 @@ def gpu_full_path(w: wl.Workload, t: dict, device="cuda", status=None):
     return out, qr, kr, cu, pos, inv_freq
 
 
+def stratified_rows(w: wl.Workload, per_long_segment: int = 2048, item_rows: int = 256, item_stride: int = 4,
+                    seed: int = 0, small_cap: int = 4096) -> np.ndarray:
+    """Rows to check at full size: every row of segments up to small_cap tokens; in longer ones
+    per_long_segment rows: the first, second, second-to-last and last rows of the segment, for every
+    item_stride-th block of item_rows query rows the first and last row of each of its two 128-row
+    halves (the first and last TMEM lane of both Q tiles of a work item), and a seeded random set
+    for the rest."""
+    rng = np.random.default_rng(seed)
+    cu = w.cu_seqlens.astype(np.int64)
+    rows = []
+    for i in range(w.num_segments):
+        a, b = int(cu[i]), int(cu[i + 1])
+        L = b - a
+        if L == 0:
+            continue
+        if L <= small_cap:
+            rows.append(np.arange(a, b))
+            continue
+        fixed = {a, a + 1, b - 2, b - 1}
+        half = item_rows // 2
+        for blk in range(0, (L + item_rows - 1) // item_rows, item_stride):
+            q0 = a + blk * item_rows
+            fixed.update({q0, q0 + half - 1, q0 + half, q0 + item_rows - 1})
+        fixed = np.array(sorted(x for x in fixed if a <= x < b))
+        assert len(fixed) <= per_long_segment
+        rest = np.setdiff1d(np.arange(a, b), fixed)
+        extra = rng.choice(rest, size=min(len(rest), per_long_segment - len(fixed)), replace=False)
+        rows.append(np.unique(np.concatenate([fixed, extra])))
+    return np.concatenate(rows) if rows else np.zeros(0, dtype=np.int64)
+
+
 def sample_rows(w: wl.Workload, big_rows: int, seed: int = 0, small_cap: int = 4096) -> np.ndarray:
     """Rows to check: every row of segments up to small_cap tokens; for longer ones the first, last,
     128-tile boundary rows and a seeded random set, big_rows in total per long segment."""

@@ -172,6 +172,32 @@ def test_padded_call_validation_without_gpu(L):
     assert padded(2, 16, 16, D=81) == -2
 
 
+def test_general_call_validation_without_gpu(L):
+    p = ctypes.c_void_p
+    O = vit._AttnOptions
+
+    def ex(cu=16, start=None, length=None, B=1, opts=None, D=80):
+        return L.vit_varlen_attn_ex(p(16), p(16), p(16), 4096, 2, D, 160, 160, 160, None if cu is None else p(cu),
+                                    None if start is None else p(start), None if length is None else p(length), B,
+                                    512, 0.0, p(16), 160, None, None, None if opts is None else ctypes.byref(opts),
+                                    p(256), 1 << 20, None, None)
+    assert ex(start=16, length=16, B=2) == -14        # both layouts at once
+    assert ex(cu=None, start=16, length=None, B=2) == -1
+    assert ex(cu=None, start=None, length=16, B=2) == -1
+    assert ex(cu=None, start=16, length=16, B=0) == 0  # padded layout with no segments: nothing to do
+    assert ex(opts=O(-2)) == -14                       # split below -1
+    assert ex(opts=O(-1), D=81) == -2
+    assert ex(cu=18) == -5                             # cu_seqlens not 4-byte aligned
+
+
+def test_release_library_exports_no_test_hook_or_global_setting(L):
+    # the failure-path hook lives only in a separate test build, and the kernel split is a
+    # per-call option: the shipped library has neither a debug call nor a process-wide knob
+    assert not hasattr(L, "vit_debug_stall_long_kernel")
+    assert not hasattr(L, "vit_set_short_segment_max")
+    assert "vit_debug_stall_long_kernel" not in open(HEADER).read()
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import importlib
     monkeypatch.setattr(vit, "_lib", None)

@@ -75,3 +75,33 @@ def test_clock_sampler_summary_and_missing_tool(tmp_path, monkeypatch):
     with bench.ClockSampler(0) as c:
         pass
     assert c.summary() is None and c.path is None
+
+
+def test_roofline_denominator_follows_the_timed_region():
+    # a contraction timed for less than SUSTAINED_AFTER_S is held to the burst peak, a longer
+    # timed region to the sustained one; both are named in the entry
+    w = wl.make_config(3)
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    kt = {"attn_long": (10, 0.5), "qk_norm_rope": (10, 0.2)}
+    short = bench.roofline_entry(None, w, kt, 64, peaks, "measured", 0.3, False)
+    long_ = bench.roofline_entry(None, w, kt, 64, peaks, "measured", 2.5, False)
+    assert short["kernel"] == "attn_long" and short["bound"] == "tensor"
+    assert short["peak"] == 1900.0 and "bf16_tflops " in short["peak_source"]
+    assert long_["peak"] == 1700.0 and "bf16_tflops_sustained" in long_["peak_source"]
+    alg = bench.kernel_algorithmic_flops(w, "attn_long", 64)
+    assert short["achieved"] == pytest.approx(alg / 0.05e-3 / 1e12)
+    assert short["frac"] == pytest.approx(short["achieved"] / 1900.0)
+    # an HBM-bound dominant kernel is held to the copy bandwidth
+    hb = bench.roofline_entry(None, w, {"qk_norm_rope": (4, 0.4)}, 64, peaks, "measured", 0.1, False)
+    assert hb["bound"] == "hbm" and hb["peak"] == 6800.0
+    assert hb["achieved"] == pytest.approx(8.0 * w.total_tokens * 16 * 80 / 0.1e-3 / 1e9)
+
+
+def test_both_arms_describe_the_same_workload():
+    import argparse
+    args = argparse.Namespace(interleaved=False, lse=False, fused_q=False)
+    w = wl.make_config(5)
+    a, b = bench.config_dict(w, args, 1), bench.config_dict(w, args, 1)
+    assert a == b and a["workload"] == w.name and a["useful_flops_per_step"] == w.useful_flops
+    assert "inputs larger than L2" in a["l2"]
+    assert "flushed" in bench.config_dict(wl.make_config(2), args, 1)["l2"]

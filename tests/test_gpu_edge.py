@@ -20,14 +20,15 @@ def _built():
     _build.build()
 
 
-SPLITS = {"default": 64, "all_long": 0, "all_short": 2 ** 31 - 1}
+# "default" passes no option (the plain entry points, the library's own split); the others pass
+# their split with every call
+SPLITS = {"default": None, "all_long": 0, "all_short": 2 ** 31 - 1}
 
 
 @pytest.fixture(params=list(SPLITS))
 def split(request):
-    prev = vit.set_short_segment_max(SPLITS[request.param])
-    yield request.param
-    vit.set_short_segment_max(prev)
+    with vit.kernel_split(SPLITS[request.param]):
+        yield request.param
 
 
 def _inputs(lengths, H, D, seed=0):
@@ -46,6 +47,27 @@ def test_segment_isolation_bitwise(D, split):
         a, b = int(cuh[seg]), int(cuh[seg + 1])
         q2, k2, v2 = q.clone(), k.clone(), v.clone()
         q2[a:b] = torch.randn_like(q2[a:b].float()).to(torch.bfloat16)
+        k2[a:b] *= -2
+        v2[a:b] += 1
+        pert = vit.varlen_attn(q2, k2, v2, cu, w.max_seqlen)
+        keep = torch.ones(w.total_tokens, dtype=torch.bool, device="cuda")
+        keep[a:b] = False
+        assert torch.equal(pert[keep].view(torch.int16), base[keep].view(torch.int16)), f"segment {seg} leaked"
+        assert not torch.equal(pert[a:b], base[a:b])
+
+
+def test_segment_isolation_bitwise_beside_a_65536_token_image(split):
+    """The headline layout: one 256x256 image (65536 tokens) packed with short images, and
+    max_seqlen padded to the 131072 bucket. Perturbing any one segment leaves every byte of
+    every other segment's output unchanged, the long neighbour included."""
+    lengths = [65536, 100, 1, 513, 64, 257]
+    w, t, cu, (q, k, v) = _inputs(lengths, 2, 80, seed=9)
+    assert w.max_seqlen == 131072
+    base = vit.varlen_attn(q, k, v, cu, w.max_seqlen).clone()
+    cuh = w.cu_seqlens
+    for seg in (0, 1, 3, 5):
+        a, b = int(cuh[seg]), int(cuh[seg + 1])
+        q2, k2, v2 = q.clone(), k.clone(), v.clone()
         k2[a:b] *= -2
         v2[a:b] += 1
         pert = vit.varlen_attn(q2, k2, v2, cu, w.max_seqlen)
@@ -177,25 +199,76 @@ def test_launches_are_counted_and_timed():
     assert "schedule" in rec and all(ms >= 0 for _, ms in rec.values())
 
 
+def _test_hooks_library():
+    """The library rebuilt with its failure-path test hook (never shipped): the release library
+    exports no debug call."""
+    import ctypes
+    L = ctypes.CDLL(_build.build_test_hooks())
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    L.vit_debug_stall_long_kernel.argtypes = [i32]
+    L.vit_debug_stall_long_kernel.restype = i32
+    L.vit_varlen_attn_ex.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, vp, vp, vp, i32, i32, f32, vp, i64,
+                                     vp, vp, ctypes.POINTER(vit._AttnOptions), vp, sz, vp, vp]
+    L.vit_varlen_attn_ex.restype = i32
+    return L
+
+
 def test_long_kernel_bounded_wait_reports_timeout_and_context_survives():
     """A wait that can never complete (V is never loaded) must end in
     VIT_ERR_TIMEOUT within its clock budget; afterwards the same process
     computes correct results again."""
+    import ctypes
     w, t, cu, (q, k, v) = _inputs([600, 300], 2, 80, seed=7)
-    prev = vit.set_short_segment_max(0)
+    L = _test_hooks_library()
+    T, H, D = q.shape
+    out = torch.empty_like(q)
+    ws = torch.empty(vit.workspace_size(T, H, w.num_segments, D), dtype=torch.uint8, device="cuda")
+    opts = vit._AttnOptions(0)                     # every segment on the tcgen05 kernel
+    p = lambda x: ctypes.c_void_p(x.data_ptr())
+
+    def call(status):
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return L.vit_varlen_attn_ex(p(q), p(k), p(v), T, H, D, q.stride(0), k.stride(0), v.stride(0), p(cu), None,
+                                    None, w.num_segments, w.max_seqlen, 0.0, p(out), out.stride(0), None, None,
+                                    ctypes.byref(opts), p(ws), ws.numel(), p(status), stream)
+
+    status = vit.new_status()
+    L.vit_debug_stall_long_kernel(1)
     try:
-        status = vit.new_status()
-        vit.debug_stall_long_kernel(True)
-        try:
-            vit.varlen_attn(q, k, v, cu, w.max_seqlen, status=status)
-            code = vit.read_status(status)
-        finally:
-            vit.debug_stall_long_kernel(False)
-        assert code == -13
-        status2 = vit.new_status()
-        out = vit.varlen_attn(q, k, v, cu, w.max_seqlen, status=status2)
-        assert vit.read_status(status2) == 0
+        assert call(status) == 0
+        code = vit.read_status(status)
     finally:
-        vit.set_short_segment_max(prev)
+        L.vit_debug_stall_long_kernel(0)
+    assert code == -13
+    status2 = vit.new_status()
+    assert call(status2) == 0
+    assert vit.read_status(status2) == 0
     ref = oracle.attention(*(oracle.widen(wl.bf16_bits(t[n])) for n in ("q", "k", "v")), w.cu_seqlens)
     assert_close(out, ref, what="after timeout")
+
+
+def test_threads_with_different_splits_get_their_own_results():
+    """The kernel split is a per-call option: two host threads that keep issuing the same
+    attention with different splits, on their own streams, each get exactly the bits their own
+    split gives when run alone (the two splits round differently, so a leaked setting shows)."""
+    import threading
+    w, t, cu, (q, k, v) = _inputs([700, 40, 300, 129], 4, 80, seed=8)
+    splits = (0, 2 ** 31 - 1)
+    alone = {sm: vit.varlen_attn(q, k, v, cu, w.max_seqlen, short_max=sm) for sm in splits}
+    torch.cuda.synchronize()
+    assert not torch.equal(alone[0], alone[splits[1]])
+    bad = []
+
+    def worker(sm):
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            outs = [vit.varlen_attn(q, k, v, cu, w.max_seqlen, short_max=sm) for _ in range(30)]
+        s.synchronize()
+        bad.extend(sm for o in outs if not torch.equal(o, alone[sm]))
+
+    th = [threading.Thread(target=worker, args=(sm,)) for sm in splits]
+    for x in th:
+        x.start()
+    for x in th:
+        x.join()
+    assert not bad

@@ -27,7 +27,9 @@ LSE_ABS = 1e-3
 # rows by several times that. There lse is held to the path's output tolerance instead.
 PATH_MAX_ABS, PATH_MEAN_ABS = 2e-2, 2e-3
 
-SPLITS = {"default": 64, "all_long": 0, "all_short": 2 ** 31 - 1}
+# "default" passes no option (the plain entry points, the library's own split); the others pass
+# their split with every call
+SPLITS = {"default": None, "all_long": 0, "all_short": 2 ** 31 - 1}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -40,9 +42,8 @@ def _built():
 
 @pytest.fixture(params=list(SPLITS))
 def split(request):
-    prev = vit.set_short_segment_max(SPLITS[request.param])
-    yield request.param
-    vit.set_short_segment_max(prev)
+    with vit.kernel_split(SPLITS[request.param]):
+        yield request.param
 
 
 def _widen(t, names=("q", "k", "v")):

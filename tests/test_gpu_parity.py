@@ -10,7 +10,7 @@ import oracle
 import vision_encoder_varlen_gb300 as vit
 from vision_encoder_varlen_gb300 import _build
 from vision_encoder_varlen_gb300 import workloads as wl
-from helpers import MAX_ABS, MEAN_ABS, assert_close, gpu_full_path, sample_rows, to_f64
+from helpers import MAX_ABS, MEAN_ABS, assert_close, gpu_full_path, stratified_rows, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -92,15 +92,17 @@ def test_full_path_parity(idx, split):
 
 
 def test_full_path_parity_mixed_long_short_sampled():
-    """The 256x256 + 7 small images case at full size: all rows of the small
-    images, and 256 rows of the 65536-token image (first/last/tile-boundary
-    rows plus a seeded random set), every head."""
+    """The 256x256 + 7 small images case at full size, in the benchmark's launch configuration:
+    all rows of the small images, and 2048 stratified rows of the 65536-token image (the first
+    and last row of both 128-row Q tiles of every 4th 256-row work item, the segment's ends,
+    and a seeded random set), every head."""
     w = wl.make_config(5)
     t = w.tensors()
     status = vit.new_status()
     out, *_ = gpu_full_path(w, t, status=status)
     assert vit.read_status(status) == 0
-    rows = sample_rows(w, big_rows=256, seed=5)
+    rows = stratified_rows(w, per_long_segment=2048, seed=5)
+    assert len(rows) >= 2048
     ref = oracle.full_path(w.grid_hw, *(wl.bf16_bits(t[n]) for n in ("q", "k", "v")),
                            wl.bf16_bits(t["norm_w"]), w.eps, w.theta, rows=rows)
     assert_close(out[torch.from_numpy(rows).cuda()], ref, what=w.name)
@@ -115,17 +117,23 @@ LENGTH_CASES = [
     ([7, 9, 2100], 2, 64),
     ([200, 33, 96, 17], 4, 96),
     ([1000], 1, 32),
+    # enough items that long blocks keep two Q tiles: the last block of 300, 513, 2000 and the
+    # single block of 100 have at most 128 rows and run as split items, those of 400 and 640 do not
+    ([300, 400, 100, 513, 640, 2000], 16, 80),
+    ([300, 1, 257, 511, 512, 513, 130], 16, 128),
+    ([129, 200, 700, 96, 1100], 12, 64),
 ]
 
 
-SPLITS = {"default": 64, "all_long": 0, "all_short": 2 ** 31 - 1}
+# "default" passes no option (the plain entry points, the library's own split); the others pass
+# their split with every call
+SPLITS = {"default": None, "all_long": 0, "all_short": 2 ** 31 - 1}
 
 
 @pytest.fixture(params=list(SPLITS))
 def split(request):
-    prev = vit.set_short_segment_max(SPLITS[request.param])
-    yield request.param
-    vit.set_short_segment_max(prev)
+    with vit.kernel_split(SPLITS[request.param]):
+        yield request.param
 
 
 @pytest.mark.parametrize("lengths,H,D", LENGTH_CASES)

@@ -1,12 +1,16 @@
 """The device scheduler's work list, bit for bit against a host recomputation.
 
 After a call, the workspace holds a 64-byte header (int32: long items, short
-items, rows per long item, rows per short item, error, tiny items) and the
-items (int4: segment start, segment length, first query row, head). The host
-recomputes the same list from the segment lengths alone: segments longer than
-the split go to the tcgen05 kernel in 256-row blocks, longest first (ties by
-index); the rest in index order, those of at most min(split, 64) tokens last,
-one item per head; heads outer, query blocks inner within a segment."""
+items, rows per long item, rows per short item, error, tiny items, whether
+every long item is split) and the items (int4: segment start, segment length,
+first query row, head | split flag). The host recomputes the same list from the
+segment lengths and the SM count alone: segments longer than the split go to
+the tcgen05 kernel in 256-row blocks, longest first (ties by index), a last
+block of at most 128 rows flagged as split; when that would give at most
+SMs / 2 long items, every long segment goes in 128-row blocks instead, all
+flagged. The rest follow in index order, those of at most min(split, 64)
+tokens last, one item per head; heads outer, query blocks inner within a
+segment."""
 import numpy as np
 import pytest
 import torch
@@ -17,6 +21,7 @@ from vision_encoder_varlen_gb300 import _build
 pytestmark = pytest.mark.gpu
 
 BM_LONG, BM_SHORT, TINY = 256, 128, 64
+SPLIT = 1 << 30
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -26,23 +31,34 @@ def _built():
     _build.build()
 
 
-def expected(lengths, starts, H, short_max):
+def expected(lengths, starts, H, short_max, num_sms):
     tiny_max = min(short_max, TINY)
     idx = range(len(lengths))
     long_s = sorted((i for i in idx if lengths[i] > short_max), key=lambda i: (-lengths[i], i))
     short_s = [i for i in idx if tiny_max < lengths[i] <= short_max]
     tiny_s = [i for i in idx if lengths[i] <= tiny_max]
+    full_items = sum(H * -(-int(lengths[i]) // BM_LONG) for i in long_s)
+    all_split = 2 * full_items <= num_sms
+    bm_long = BM_LONG // 2 if all_split else BM_LONG
     items, counts = [], []
-    for group, bm in ((long_s, BM_LONG), (short_s, BM_SHORT), (tiny_s, BM_SHORT)):
+    for group, bm in ((long_s, bm_long), (short_s, BM_SHORT), (tiny_s, BM_SHORT)):
         n0 = len(items)
         for seg in group:
             L, a = int(lengths[seg]), int(starts[seg])
+            if L == 0:
+                continue
             nq = (L + bm - 1) // bm
             for h in range(H):
                 for qb in range(nq):
-                    items.append((a, L, a + qb * bm, h))
+                    last_rows = L - qb * bm
+                    split = group is long_s and (all_split or (qb == nq - 1 and 2 * last_rows <= BM_LONG))
+                    items.append((a, L, a + qb * bm, h | (SPLIT if split else 0)))
         counts.append(len(items) - n0)
-    return counts, np.array(items, dtype=np.int32).reshape(-1, 4)
+    return counts, np.array(items, dtype=np.int32).reshape(-1, 4), bm_long, all_split
+
+
+def _num_sms():
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
 
 
 def run(lengths, H, D, short_max, padded=False):
@@ -60,8 +76,7 @@ def run(lengths, H, D, short_max, padded=False):
     B = len(lengths)
     q = torch.zeros((max(T, 1), H, D), dtype=torch.bfloat16, device="cuda")[:T]
     ws = torch.zeros(vit.workspace_size(T, H, B, D), dtype=torch.uint8, device="cuda")
-    prev = vit.set_short_segment_max(short_max)
-    try:
+    with vit.kernel_split(short_max):
         status = vit.new_status()
         if padded:
             vit.varlen_attn_padded(q, q, q, torch.from_numpy(starts.astype(np.int32)).cuda(),
@@ -71,8 +86,6 @@ def run(lengths, H, D, short_max, padded=False):
             cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)).cuda()
             vit.varlen_attn(q, q, q, cu, max(int(lengths.max()), 1), workspace=ws, status=status)
         assert vit.read_status(status) == 0
-    finally:
-        vit.set_short_segment_max(prev)
     raw = ws.cpu().numpy()
     hdr = raw[:64].view(np.int32)
     return hdr, raw[64:].view(np.int32).reshape(-1, 4), starts
@@ -82,6 +95,9 @@ CASES = [
     ([300, 1, 0, 64, 65, 2000, 129, 128, 17, 0, 700], 3),
     ([5, 4096, 4096, 4095, 1], 2),
     ([64] * 50 + [65] * 7 + [1000] * 3, 1),
+    ([1024], 16),                                   # one 32x32 image: few items, all split
+    ([1000, 129, 300], 8),                          # exactly at the all-split threshold region
+    ([200, 90, 65], 1),
 ]
 
 
@@ -90,12 +106,24 @@ CASES = [
 @pytest.mark.parametrize("lengths,H", CASES)
 def test_work_list_matches_host_recomputation(lengths, H, short_max, padded):
     hdr, items, starts = run(lengths, H, 80, short_max, padded)
-    counts, ref = expected(np.asarray(lengths), starts, H, short_max)
+    counts, ref, bm_long, all_split = expected(np.asarray(lengths), starts, H, short_max, _num_sms())
     n = sum(counts)
     assert hdr[4] == 0                                     # no error
     assert (hdr[0], hdr[1], hdr[5]) == tuple(counts)
-    assert (hdr[2], hdr[3]) == (BM_LONG, BM_SHORT)
+    if counts[0]:
+        assert hdr[2] == bm_long and hdr[6] == int(all_split)
+    assert hdr[3] == BM_SHORT
     assert np.array_equal(items[:n], ref)
+
+
+def test_small_batches_are_cut_into_split_items():
+    # 16 heads of one 1024-token image: 64 two-tile items would leave most SMs idle, so the
+    # scheduler cuts 128 split items of 128 rows instead (up to 152 SMs)
+    if _num_sms() < 128:
+        pytest.skip("needs at least 128 SMs")
+    hdr, items, _ = run([1024], 16, 80, 64)
+    assert hdr[0] == 128 and hdr[2] == 128 and hdr[6] == 1
+    assert np.all(items[:128, 3] & SPLIT)
 
 
 def test_work_list_many_segments():
@@ -103,6 +131,6 @@ def test_work_list_many_segments():
     lengths = rng.integers(0, 300, size=3000)
     lengths[rng.choice(3000, 20, replace=False)] = rng.integers(1000, 5000, size=20)
     hdr, items, starts = run(lengths, 2, 64, 64)
-    counts, ref = expected(lengths, starts, 2, 64)
+    counts, ref, _, _ = expected(lengths, starts, 2, 64, _num_sms())
     assert (hdr[0], hdr[1], hdr[5]) == tuple(counts)
     assert np.array_equal(items[:sum(counts)], ref)

@@ -11,6 +11,7 @@ library is not built, every call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -36,6 +37,10 @@ class VitError(RuntimeError):
 class _QRope(ctypes.Structure):
     _fields_ = [("pos_hw", ctypes.c_void_p), ("cos_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int),
                 ("norm_w", ctypes.c_void_p), ("eps", ctypes.c_float), ("rope_mode", ctypes.c_int)]
+
+
+class _AttnOptions(ctypes.Structure):
+    _fields_ = [("short_segment_max", ctypes.c_int)]
 
 
 class _KernelTime(ctypes.Structure):
@@ -71,21 +76,40 @@ def lib() -> ctypes.CDLL:
             L.vit_rope_table.argtypes = [vp, i32, i32, vp, vp]
             L.vit_varlen_attn_padded.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, vp, vp, i32, i32, f32, vp,
                                                  i64, vp, ctypes.POINTER(_QRope), vp, sz, vp, vp]
+            L.vit_varlen_attn_ex.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, vp, vp, vp, i32, i32, f32, vp,
+                                             i64, vp, ctypes.POINTER(_QRope), ctypes.POINTER(_AttnOptions), vp, sz,
+                                             vp, vp]
             L.vit_read_status.argtypes = [vp, vp]
-            L.vit_set_short_segment_max.argtypes = [i32]
-            L.vit_set_short_segment_max.restype = i32
-            L.vit_debug_stall_long_kernel.argtypes = [i32]
-            L.vit_debug_stall_long_kernel.restype = i32
             L.vit_launch_count.restype = i64
             L.vit_kernel_timing.argtypes = [i32]
             L.vit_kernel_timing_read.argtypes = [ctypes.POINTER(_KernelTime), i32]
             for fn in ("vit_device_supported", "vit_rope_freqs", "vit_qk_norm_rope", "vit_qk_norm_rope_ex",
                        "vit_varlen_attn", "vit_varlen_attn_lse", "vit_varlen_attn_fused_q", "vit_rope_table",
-                       "vit_varlen_attn_padded",
+                       "vit_varlen_attn_padded", "vit_varlen_attn_ex",
                        "vit_read_status", "vit_kernel_timing", "vit_kernel_timing_read"):
                 getattr(L, fn).restype = i32
             _lib = L
     return _lib
+
+
+_tls = threading.local()
+
+
+@contextlib.contextmanager
+def kernel_split(short_max: int | None):
+    """Within the block, attention calls made by this thread pass ``short_max`` as their kernel
+    split (segments longer than it run on the tcgen05 kernel); None restores the library default.
+    Per thread, and passed with every call: the library itself keeps no setting between calls."""
+    prev = getattr(_tls, "short_max", None)
+    _tls.short_max = None if short_max is None else int(short_max)
+    try:
+        yield
+    finally:
+        _tls.short_max = prev
+
+
+def _split(short_max):
+    return short_max if short_max is not None else getattr(_tls, "short_max", None)
 
 
 def status_string(code: int) -> str:
@@ -208,17 +232,28 @@ def _max_seqlen(m) -> int:
     return 0 if m is None else int(m)
 
 
+def _attn_ex(q, k, v, qs, ks, vs, cu_seqlens, seq_start, seq_len, B, max_seqlen, scale, out, os_, lse, qr,
+             short_max, workspace, status, stream, what):
+    opts = _AttnOptions(int(short_max))
+    _check(lib().vit_varlen_attn_ex(_ptr(q), _ptr(k), _ptr(v), q.shape[0], q.shape[1], q.shape[2], qs, ks, vs,
+                                    _ptr(cu_seqlens), _ptr(seq_start), _ptr(seq_len), B, _max_seqlen(max_seqlen),
+                                    float(scale) if scale is not None else 0.0, _ptr(out), os_, _ptr(lse),
+                                    ctypes.byref(qr) if qr is not None else None, ctypes.byref(opts),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+                                    _stream(stream)), what)
+
+
 def varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor | None,
                 max_seqlen: int | None = None, scale: float | None = None, *, num_segments: int | None = None,
                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                 status: torch.Tensor | None = None, return_lse: bool = False, lse: torch.Tensor | None = None,
-                stream=None):
+                short_max: int | None = None, stream=None):
     """Non-causal attention inside each packed segment. q, k, v [T, H, D] bf16 -> out [T, H, D] bf16.
 
     ``max_seqlen`` bounds the segment lengths (a padded bucket is fine); None leaves the bound
     to the library (T), so nothing is read back to the host. With ``return_lse`` (or an ``lse``
     buffer) also returns lse [T, H] fp32, the natural-log sum of exp(scale * q.k) over each
-    row's segment: (out, lse)."""
+    row's segment: (out, lse). ``short_max`` is this call's kernel split (see kernel_split)."""
     T, H, D = q.shape
     qs, ks, vs = _tok_stride(q, "q", H, D), _tok_stride(k, "k", H, D), _tok_stride(v, "v", H, D)
     if cu_seqlens is not None:
@@ -237,15 +272,21 @@ def varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: t
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     sc = float(scale) if scale is not None else 0.0
     ws_bytes = workspace.numel() * workspace.element_size()
-    if not return_lse and lse is None:
+    short_max = _split(short_max)
+    if return_lse and lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (T, H) or not lse.is_contiguous()
+                            or not lse.is_cuda):
+        raise ValueError(f"lse must be a contiguous CUDA float32 tensor [{T}, {H}]")
+    if short_max is not None:
+        _attn_ex(q, k, v, qs, ks, vs, cu_seqlens, None, None, B, max_seqlen, scale, out, os_, lse, None, short_max,
+                 workspace, status, stream, "vit_varlen_attn_ex")
+        return (out, lse) if lse is not None else out
+    if lse is None:
         _check(lib().vit_varlen_attn(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, _ptr(cu_seqlens), B,
                                      _max_seqlen(max_seqlen), sc, _ptr(out), os_, _ptr(workspace), ws_bytes,
                                      _ptr(status), _stream(stream)), "vit_varlen_attn")
         return out
-    if lse is None:
-        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (T, H) or not lse.is_contiguous() or not lse.is_cuda:
-        raise ValueError(f"lse must be a contiguous CUDA float32 tensor [{T}, {H}]")
     _check(lib().vit_varlen_attn_lse(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, _ptr(cu_seqlens), B,
                                      _max_seqlen(max_seqlen), sc, _ptr(out), os_, _ptr(lse), _ptr(workspace), ws_bytes,
                                      _ptr(status), _stream(stream)), "vit_varlen_attn_lse")
@@ -258,7 +299,7 @@ def varlen_attn_fused_q(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_se
                         interleaved: bool = False, num_segments: int | None = None,
                         out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                         status: torch.Tensor | None = None, return_lse: bool = False,
-                        lse: torch.Tensor | None = None, stream=None):
+                        lse: torch.Tensor | None = None, short_max: int | None = None, stream=None):
     """varlen_attn on raw q: the kernels normalise (q_norm_w [D], or None) and rotate every Q tile
     after loading it. k must already be normalised and rotated (qk_norm_rope(None, k, ...))."""
     T, H, D = q.shape
@@ -289,6 +330,11 @@ def varlen_attn_fused_q(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_se
     qr = _QRope(pos_hw.data_ptr(), cos_sin.data_ptr(), int(cos_sin.shape[0]),
                 q_norm_w.data_ptr() if q_norm_w is not None else None, float(eps),
                 ROPE_INTERLEAVED if interleaved else ROPE_ROTATE_HALF)
+    short_max = _split(short_max)
+    if short_max is not None:
+        _attn_ex(q, k, v, qs, ks, vs, cu_seqlens, None, None, B, max_seqlen, scale, out, os_, lse, qr, short_max,
+                 workspace, status, stream, "vit_varlen_attn_ex")
+        return (out, lse) if lse is not None else out
     _check(lib().vit_varlen_attn_fused_q(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, ctypes.byref(qr),
                                          _ptr(cu_seqlens), B, _max_seqlen(max_seqlen),
                                          float(scale) if scale is not None else 0.0, _ptr(out), os_, _ptr(lse),
@@ -300,7 +346,8 @@ def varlen_attn_fused_q(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_se
 def varlen_attn_padded(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_start: torch.Tensor,
                        seq_len: torch.Tensor, max_seqlen: int | None = None, scale: float | None = None, *,
                        out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                       status: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+                       status: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                       short_max: int | None = None, stream=None):
     """Attention over a padded layout: segment i is rows [seq_start[i], seq_start[i] + seq_len[i]) of
     q, k, v and out (ascending, not overlapping); rows between segments are left untouched. Nothing
     on the host depends on the lengths, so the call can be captured in a CUDA graph and replayed
@@ -320,6 +367,11 @@ def varlen_attn_padded(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_st
         workspace = torch.empty(max(workspace_size(T, H, B, D), 16), dtype=torch.uint8, device=q.device)
     if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (T, H) or not lse.is_contiguous()):
         raise ValueError(f"lse must be a contiguous CUDA float32 tensor [{T}, {H}]")
+    short_max = _split(short_max)
+    if short_max is not None:
+        _attn_ex(q, k, v, qs, ks, vs, None, seq_start, seq_len, B, max_seqlen, scale, out, os_, lse, None, short_max,
+                 workspace, status, stream, "vit_varlen_attn_ex")
+        return out
     _check(lib().vit_varlen_attn_padded(_ptr(q), _ptr(k), _ptr(v), T, H, D, qs, ks, vs, _ptr(seq_start),
                                         _ptr(seq_len), B, _max_seqlen(max_seqlen),
                                         float(scale) if scale is not None else 0.0, _ptr(out), os_, _ptr(lse), None,
@@ -344,15 +396,7 @@ def encoder_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: 
                                interleaved=interleaved, **kw)
 
 
-def set_short_segment_max(short_max: int) -> int:
-    """Segments longer than short_max go to the tcgen05 long-segment kernel (default 64).
-    Returns the previous value."""
-    return int(lib().vit_set_short_segment_max(int(short_max)))
-
-
-def debug_stall_long_kernel(enable: bool) -> bool:
-    """Test hook: make the long-segment kernel's bounded waits expire (VIT_ERR_TIMEOUT)."""
-    return bool(lib().vit_debug_stall_long_kernel(1 if enable else 0))
+DEFAULT_SHORT_MAX = 64   # the library's kernel split when a call passes none
 
 
 def launch_count() -> int:

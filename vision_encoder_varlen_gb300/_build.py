@@ -20,6 +20,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libvitattn.so")
+# the same library with the failure-path test hook compiled in (tests only; never loaded by the product)
+TEST_LIB = os.path.join(LIBDIR, "libvitattn_testhooks.so")
+TEST_HOOK_SOURCES = ("api.cu",)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -84,6 +87,33 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         raise RuntimeError(f"nvcc link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
     return LIB
+
+
+def build_test_hooks() -> str:
+    """Build TEST_LIB: the release objects, with the translation units that hold the test hook
+    (TEST_HOOK_SOURCES) compiled again with VIT_TEST_HOOKS defined."""
+    build()
+    if os.path.exists(TEST_LIB) and os.path.getmtime(TEST_LIB) >= os.path.getmtime(LIB):
+        return TEST_LIB
+    nvcc = _nvcc()
+    objs = []
+    for src in _sources():
+        name = os.path.basename(src)
+        if name in TEST_HOOK_SOURCES:
+            obj = os.path.join(BUILD, name + ".testhooks.o")
+            r = subprocess.run([nvcc, *compile_flags(), "-DVIT_TEST_HOOKS", "-c", src, "-o", obj],
+                               capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"nvcc failed for {name} (test hooks):\n{r.stderr}")
+        else:
+            obj = os.path.join(BUILD, name + ".o")
+        objs.append(obj)
+    tmp = TEST_LIB + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc link failed (test hooks):\n{r.stderr}")
+    os.replace(tmp, TEST_LIB)
+    return TEST_LIB
 
 
 if __name__ == "__main__":

@@ -56,11 +56,18 @@ vit_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? VIT_OK : VIT_E
 constexpr int64_t kMaxTokens = (int64_t)1 << 31;
 
 // Segments longer than this run on the tcgen05 long-segment kernel, the others on the
-// warp-MMA kernels. Measured on GB300: up to 64 tokens the tiny-segment kernel is 2-4x
-// faster than the tcgen05 kernel, from 64 tokens up the tcgen05 kernel wins.
-std::atomic<int> g_short_max{64};
-// Test hook: when set, the long-segment kernel never loads V, so its bounded waits expire.
+// warp-MMA kernels, unless a call's options say otherwise. Measured on GB300: up to 64 tokens
+// the tiny-segment kernel is 2-4x faster than the tcgen05 kernel, from 64 tokens up the
+// tcgen05 kernel wins.
+constexpr int kDefaultShortMax = 64;
+
+#ifdef VIT_TEST_HOOKS
+// Test builds only: when set, the long-segment kernel never loads V, so its bounded waits expire.
 std::atomic<int> g_stall_v{0};
+int stall_v() { return stall_v(); }
+#else
+constexpr int stall_v() { return 0; }
+#endif
 
 }  // namespace
 
@@ -195,24 +202,27 @@ size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D)
 
 }  // extern "C"
 
-namespace {
+namespace vit {
 
-vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64_t T, int H, int D, int64_t q_stride,
-                              int64_t k_stride, int64_t v_stride, const vit_q_rope_t *q_rope,
-                              const int32_t *cu_seqlens, const int32_t *seq_start, const int32_t *seq_len, int B,
-                              int max_seqlen, float scale, void *out, int64_t out_stride, float *lse,
-                              void *workspace, size_t workspace_bytes, int32_t *status_dev, vit_stream_t stream)
+// Every host-side check of the attention calls except those of the workspace.
+// *nothing is set when the call has no work at all (no segments and no tokens).
+vit_status_t check_varlen_attn_args(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                    int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                                    const vit_q_rope_t *q_rope, const int32_t *cu_seqlens, const int32_t *seq_start,
+                                    const int32_t *seq_len, int B, int max_seqlen, float scale, const void *out,
+                                    int64_t out_stride, const float *lse, const vit_attn_options_t *opts,
+                                    bool *nothing)
 {
     const bool padded = seq_len != nullptr;
+    *nothing = false;
     if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
-    if (T < 0 || T >= kMaxTokens || H < 1 || B < 0) return VIT_ERR_BAD_SHAPE;
+    if (T < 0 || T >= kMaxTokens || H < 1 || H >= kMaxHeads || B < 0) return VIT_ERR_BAD_SHAPE;
     if (B > VIT_MAX_SEGMENTS) return VIT_ERR_TOO_MANY_SEGMENTS;
-    if (B == 0) return T == 0 ? VIT_OK : VIT_ERR_BAD_SHAPE;
+    if (B == 0) {
+        *nothing = T == 0;
+        return T == 0 ? VIT_OK : VIT_ERR_BAD_SHAPE;
+    }
     if (max_seqlen < 0) return VIT_ERR_BAD_ARGUMENT;
-    // 0 = not given: every segment lies inside [0, T), so T bounds it. ([TS] _varlen_metadata
-    // derives the exact maximum with a device-to-host read instead; a bound is all that is
-    // needed here, and taking T keeps the call free of host synchronisation.)
-    if (max_seqlen == 0) max_seqlen = (int)T;
     if (isnan(scale) || isinf(scale)) return VIT_ERR_BAD_ARGUMENT;
     if (padded) {
         if (!seq_start) return VIT_ERR_NULL_POINTER;
@@ -220,6 +230,7 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
     } else if (!cu_seqlens && T % B != 0) {
         return VIT_ERR_BAD_ARGUMENT;
     }
+    if ((uintptr_t)cu_seqlens & 3u) return VIT_ERR_MISALIGNED;
     if (T > 0) {
         if (!q || !k || !v || !out) return VIT_ERR_NULL_POINTER;
         if (!stride_ok(q_stride, H, D) || !stride_ok(k_stride, H, D) || !stride_ok(v_stride, H, D) ||
@@ -237,14 +248,40 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
         if (((uintptr_t)q_rope->pos_hw & 7u) || !aligned16(q_rope->cos_sin) || !aligned16(q_rope->norm_w))
             return VIT_ERR_MISALIGNED;
     }
+    if (opts && opts->short_segment_max < -1) return VIT_ERR_BAD_ARGUMENT;
+    if (vit_varlen_attn_workspace_size(T, H, B, D) == 0) return VIT_ERR_BAD_SHAPE;
+    return VIT_OK;
+}
+
+vit_status_t check_device() { return device_info(nullptr); }
+
+}  // namespace vit
+
+namespace {
+
+vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64_t T, int H, int D, int64_t q_stride,
+                              int64_t k_stride, int64_t v_stride, const vit_q_rope_t *q_rope,
+                              const int32_t *cu_seqlens, const int32_t *seq_start, const int32_t *seq_len, int B,
+                              int max_seqlen, float scale, void *out, int64_t out_stride, float *lse,
+                              const vit_attn_options_t *opts, void *workspace, size_t workspace_bytes,
+                              int32_t *status_dev, vit_stream_t stream)
+{
+    const bool padded = seq_len != nullptr;
+    bool nothing = false;
+    vit_status_t st = check_varlen_attn_args(q, k, v, T, H, D, q_stride, k_stride, v_stride, q_rope, cu_seqlens,
+                                             seq_start, seq_len, B, max_seqlen, scale, out, out_stride, lse, opts,
+                                             &nothing);
+    if (st != VIT_OK || nothing) return st;
+    // 0 = not given: every segment lies inside [0, T), so T bounds it. ([TS] _varlen_metadata
+    // derives the exact maximum with a device-to-host read instead; a bound is all that is
+    // needed here, and taking T keeps the call free of host synchronisation.)
+    if (max_seqlen == 0) max_seqlen = (int)T;
     if (!workspace) return VIT_ERR_NULL_POINTER;
-    if (!aligned16(workspace) || ((uintptr_t)cu_seqlens & 3u)) return VIT_ERR_MISALIGNED;
-    const size_t need = vit_varlen_attn_workspace_size(T, H, B, D);
-    if (need == 0) return VIT_ERR_BAD_SHAPE;
-    if (workspace_bytes < need) return VIT_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return VIT_ERR_MISALIGNED;
+    if (workspace_bytes < vit_varlen_attn_workspace_size(T, H, B, D)) return VIT_ERR_WORKSPACE_TOO_SMALL;
 
     int sms = 0;
-    vit_status_t st = device_info(&sms);
+    st = device_info(&sms);
     if (st != VIT_OK) return st;
     if (scale <= 0.f) scale = 1.0f / sqrtf((float)D);
     cudaStream_t s = (cudaStream_t)stream;
@@ -252,10 +289,11 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
     WsHeader *hdr = static_cast<WsHeader *>(workspace);
     Item *items = reinterpret_cast<Item *>(hdr + 1);
     SchedParams sp;
-    sp.short_max = g_short_max.load();
+    sp.short_max = (opts && opts->short_segment_max >= 0) ? opts->short_segment_max : kDefaultShortMax;
     sp.tiny_max = sp.short_max < attn_tiny_max() ? sp.short_max : attn_tiny_max();
     sp.bm_long = attn_long_bm();
     sp.bm_short = attn_short_bm();
+    sp.num_sms = sms;
     // the scheduler divides by these with shifts
     if ((sp.bm_long & (sp.bm_long - 1)) || (sp.bm_short & (sp.bm_short - 1))) return VIT_ERR_BAD_ARGUMENT;
     cudaError_t e = launch_schedule(padded ? nullptr : cu_seqlens, seq_start, seq_len, B, T, H, max_seqlen, sp, hdr,
@@ -293,7 +331,8 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
     // a segment can only be long when the bound allows it
     const int64_t longest = (cu_seqlens || padded) ? (int64_t)max_seqlen : T / B;
     if (longest > sp.short_max) {
-        e = launch_attn_long(a, max_items(T, H, B, sp.bm_long), sms, g_stall_v.load(), s);
+        // split items cover bm_long / 2 rows, so that many more items may exist
+        e = launch_attn_long(a, max_items(T, H, B, sp.bm_long / 2), sms, stall_v(), s);
         if (e != cudaSuccess) return VIT_ERR_CUDA;
     }
     // segments in (tiny_max, short_max] on the short-segment kernel, the rest of the short ones
@@ -317,7 +356,8 @@ vit_status_t vit_varlen_attn_lse(const void *q, const void *k, const void *v, in
 {
     TraceRange trace("vit_varlen_attn_lse");
     return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, nullptr, cu_seqlens, nullptr, nullptr, B,
-                            max_seqlen, scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
+                            max_seqlen, scale, out, out_stride, lse, nullptr, workspace, workspace_bytes, status_dev,
+                            stream);
 }
 
 vit_status_t vit_varlen_attn_fused_q(const void *q, const void *k, const void *v, int64_t T, int H, int D,
@@ -329,7 +369,8 @@ vit_status_t vit_varlen_attn_fused_q(const void *q, const void *k, const void *v
     TraceRange trace("vit_varlen_attn_fused_q");
     if (!q_rope) return VIT_ERR_NULL_POINTER;
     return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, q_rope, cu_seqlens, nullptr, nullptr, B,
-                            max_seqlen, scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
+                            max_seqlen, scale, out, out_stride, lse, nullptr, workspace, workspace_bytes, status_dev,
+                            stream);
 }
 
 vit_status_t vit_varlen_attn_padded(const void *q, const void *k, const void *v, int64_t T, int H, int D,
@@ -344,7 +385,8 @@ vit_status_t vit_varlen_attn_padded(const void *q, const void *k, const void *v,
     if (B == 0) return VIT_OK;                           // every row is padding: nothing to compute
     if (!seq_len || !seq_start) return VIT_ERR_NULL_POINTER;
     return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, q_rope, nullptr, seq_start, seq_len, B,
-                            max_seqlen, scale, out, out_stride, lse, workspace, workspace_bytes, status_dev, stream);
+                            max_seqlen, scale, out, out_stride, lse, nullptr, workspace, workspace_bytes, status_dev,
+                            stream);
 }
 
 vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_t T, int H, int D, int64_t q_stride,
@@ -354,18 +396,36 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
 {
     TraceRange trace("vit_varlen_attn");
     return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, nullptr, cu_seqlens, nullptr, nullptr, B,
-                            max_seqlen, scale, out, out_stride, nullptr, workspace, workspace_bytes, status_dev, stream);
+                            max_seqlen, scale, out, out_stride, nullptr, nullptr, workspace, workspace_bytes, status_dev,
+                            stream);
 }
 
+vit_status_t vit_varlen_attn_ex(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                int64_t q_stride, int64_t k_stride, int64_t v_stride, const int32_t *cu_seqlens,
+                                const int32_t *seq_start, const int32_t *seq_len, int B, int max_seqlen, float scale,
+                                void *out, int64_t out_stride, float *lse, const vit_q_rope_t *q_rope,
+                                const vit_attn_options_t *opts, void *workspace, size_t workspace_bytes,
+                                int32_t *status_dev, vit_stream_t stream)
+{
+    TraceRange trace("vit_varlen_attn_ex");
+    if (seq_len || seq_start) {
+        if (cu_seqlens) return VIT_ERR_BAD_ARGUMENT;   // one layout or the other
+        if (!head_dim_ok(D)) return VIT_ERR_BAD_HEAD_DIM;
+        if (T < 0 || T >= kMaxTokens || H < 1 || B < 0) return VIT_ERR_BAD_SHAPE;
+        if (B == 0) return VIT_OK;
+        if (!seq_len || !seq_start) return VIT_ERR_NULL_POINTER;
+    }
+    return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, q_rope, cu_seqlens, seq_start, seq_len, B,
+                            max_seqlen, scale, out, out_stride, lse, opts, workspace, workspace_bytes, status_dev,
+                            stream);
+}
+
+#ifdef VIT_TEST_HOOKS
 int vit_debug_stall_long_kernel(int enable)
 {
     return g_stall_v.exchange(enable ? 1 : 0);
 }
-
-int vit_set_short_segment_max(int short_max)
-{
-    return g_short_max.exchange(short_max < 0 ? 0 : short_max);
-}
+#endif
 
 vit_status_t vit_read_status(const int32_t *status_dev, vit_stream_t stream)
 {

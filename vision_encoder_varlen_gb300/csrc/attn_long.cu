@@ -7,7 +7,11 @@
 // P.V product, fp32 accumulation in TMEM, bf16 output.
 //
 // One work item = (segment, head, 256 query rows) = two 128-row Q tiles that
-// share every K/V tile the TMA warp streams in. Persistent CTAs (one per SM)
+// share every K/V tile the TMA warp streams in; or, flagged split, (segment,
+// head, 128 query rows): one Q tile whose key tiles alternate between the two
+// halves of the CTA, which merge their partial results at the end (the
+// segment's last block when it has at most 128 rows, and every block of a
+// batch too small to occupy the GPU otherwise). Persistent CTAs (one per SM)
 // walk the scheduler's longest-first list. Three warpgroups (384 threads,
 // launched at 168 registers; setmaxnreg lowers the control warpgroup to 88
 // and raises the two softmax warpgroups to 208):
@@ -28,7 +32,9 @@
 //   warps 8-11  softmax group 1 (tile 1)  thread: row max, lazy rescaling of
 //               O (only when the max grows by more than 2^8), exp2 with the
 //               scale folded in, row sum, P -> bf16 into the tile's own P
-//               region of TMEM, and the epilogue O / l -> bf16 -> HBM.
+//               region of TMEM, and the epilogue O / l -> bf16 -> HBM (for a
+//               split item, both groups combine O0 and O1 with their maxima
+//               and sums, each writing half of the head's columns).
 // TMEM (512 columns): S0 | S1 | O0 | O1 | P0 | P1; the key tile BN is the
 // largest that fits (128 for head_dim <= 64, 112 for 80, 96 for 96, 80 for
 // 128), so the two tiles never wait for each other. Keys past the segment end are
@@ -58,14 +64,17 @@ constexpr int kSoftmaxRegs = 208;             // softmax warpgroups after setmax
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split exceeds the launch pool");
 constexpr int BM = 128;                       // rows per Q tile; two tiles per item
 constexpr long long kWaitBudget = 4000000000ll;   // clock cycles before a wait gives up (~2 s)
+constexpr int kItemRing = 4;                  // items the producer may publish ahead of the other roles
+constexpr int kItemReaders = 11;              // the two issuers, warp 3 and the eight softmax warps
 
 template <int D> struct LongCfg {
     // keys per tile: the largest multiple of 16 (at most 128) with S0, S1 (BN columns each),
     // O0, O1 (D each) and separate P0, P1 (BN/2 each) inside the 512 TMEM columns
     static constexpr int BN = ((512 - 2 * D) / 3 / 16 * 16 > 128) ? 128 : (512 - 2 * D) / 3 / 16 * 16;
-    // K/V ring of 3 slots; the next item's Q pair is prefetched into a second Q buffer
-    // where that still fits in shared memory (all head dims but 128)
-    static constexpr int STAGES = 3;
+    // K/V ring of 3 slots (2 at head_dim 128, where three would leave no room for a second Q
+    // buffer); the next item's Q pair is prefetched into a second Q buffer where that fits in
+    // shared memory (every supported head dim)
+    static constexpr int STAGES = D >= 128 ? 2 : 3;
     static constexpr int QBUF =
         (4 * (D / 16) * BM * 32 + STAGES * 2 * (D / 16) * BN * 32 + 1024 <= 227 * 1024) ? 2 : 1;
     static constexpr int NSLAB = D / 16;
@@ -94,6 +103,8 @@ struct Bars {
     uint64_t k_full[3], v_full[3], kv_empty[3];
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
     uint64_t drain[2];
+    uint64_t merge;          // split items: the eight softmax warps meet twice at the item's end
+    uint64_t item_full[kItemRing], item_empty[kItemRing];   // the producer's item ring
 };
 
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_addr(&b); }
@@ -129,7 +140,7 @@ template <int D, bool LSE, bool FQ>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out, int64_t out_stride,
-                 float *__restrict__ lse, int H, float scale_log2, const WsHeader *__restrict__ hdr,
+                 float *__restrict__ lse, int H, float scale_log2, WsHeader *__restrict__ hdr,
                  const Item *__restrict__ items, int32_t *status, int stall_v, const rope::QRope qr)
 {
     using C = LongCfg<D>;
@@ -139,9 +150,11 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __shared__ Bars bars;
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
+    __shared__ float s_m[2][BM], s_l[2][BM];   // split items: each half's running max and row sum per row
+    __shared__ Item s_items[kItemRing];        // the item ring (y < 0: the end of this CTA's list)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = hdr->n_long;
+    const int n_items = hdr->n_long;                   // read by the producer; the others take items from it
 
     if (threadIdx.x == 0) {
         s_abort = 0;
@@ -164,6 +177,11 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         mbar_init(bar_addr(bars.drain[0]), 1);
         mbar_init(bar_addr(bars.drain[1]), 1);
+        mbar_init(bar_addr(bars.merge), 8);
+        for (int r = 0; r < kItemRing; ++r) {
+            mbar_init(bar_addr(bars.item_full[r]), 1);
+            mbar_init(bar_addr(bars.item_empty[r]), kItemReaders);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -191,6 +209,17 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     auto wait_warp = [&](const uint64_t &b, uint32_t parity) -> bool {
         return __all_sync(0xffffffffu, wait(b, parity)) != 0;
     };
+    // The k-th item of this CTA from the producer's ring: false at the end of the list or when a
+    // wait gave up. Called by one thread (issuers) or by a whole warp (warp_wide); one arrival per
+    // caller frees the slot once its item has been copied out.
+    auto take_item = [&](uint32_t k, Item &x, bool warp_wide, bool &ok_) -> bool {
+        const uint32_t slot = k % kItemRing, par = (k / kItemRing) & 1;
+        if (!(ok_ = warp_wide ? wait_warp(bars.item_full[slot], par) : wait(bars.item_full[slot], par))) return false;
+        x = s_items[slot];
+        if (warp_wide) __syncwarp();
+        if (!warp_wide || lane == 0) mbar_arrive(bar_addr(bars.item_empty[slot]));
+        return x.y >= 0;
+    };
 
     if (warp < 4) regs_dec<kCtrlRegs>();
     if (warp == 0) {
@@ -204,9 +233,11 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // two bits per stage, kept in registers
             uint32_t q_pend = 0, k_pend = 0, v_pend = 0;     // q_pend: two bits per Q buffer
             bool ok = true;
-            auto load_q = [&](uint32_t qb, uint32_t qn, int q0, int head) {
-                mbar_arrive_expect_tx(bar_addr(bars.q_full[qb]), 2 * C::Q_TILE);
-                for (int i = 0; i < 2; ++i)
+            // a split item has one Q tile, the other items two
+            auto load_q = [&](uint32_t qb, uint32_t qn, int q0, int head, bool split) {
+                const int nt = split ? 1 : 2;
+                mbar_arrive_expect_tx(bar_addr(bars.q_full[qb]), nt * C::Q_TILE);
+                for (int i = 0; i < nt; ++i)
                     for (int s = 0; s < NSLAB; ++s)
                         tma_load_2d(smem_addr(base + C::OFF_Q + (2 * qb + i) * C::Q_TILE + s * C::Q_SLAB), &tm_q,
                                     head * D + 16 * s, q0 + BM * i, bar_addr(bars.q_full[qb]));
@@ -215,26 +246,42 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // raw Q needs time for warp 3 to rotate it, so with two Q buffers the next item's Q
             // goes out as soon as its buffer is free rather than after this item's last K/V tile
             bool q_early = false;                            // Q of item q_it already issued
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++q_it) {
-                const Item item = items[it];
-                const int seg0 = item.x, seg_len = item.y, q0 = item.z, head = item.w;
+            // Items: the CTA's first is its block index; each later one is taken from a device-wide
+            // counter, so a CTA that finishes early takes the next item of the longest-first list
+            // (greedy list scheduling). Each is published to the other roles through the ring.
+            uint32_t k_pub = 0;
+            auto publish = [&](const Item &x) -> bool {
+                const uint32_t slot = k_pub % kItemRing;
+                if (k_pub >= kItemRing && !(ok = wait(bars.item_empty[slot], (k_pub / kItemRing - 1) & 1)))
+                    return false;
+                s_items[slot] = x;
+                mbar_arrive(bar_addr(bars.item_full[slot]));
+                ++k_pub;
+                return true;
+            };
+            const Item kEnd = make_int4(0, -1, 0, 0);
+            int it = blockIdx.x;
+            Item item = it < n_items ? items[it] : kEnd;
+            for (; ok && it < n_items; ++q_it) {
+                if (!publish(item)) break;
+                const int it_next = (int)gridDim.x + atomicAdd(&hdr->next_long, 1);
+                const Item nx = it_next < n_items ? items[it_next] : kEnd;
+                const int seg0 = item.x, seg_len = item.y, q0 = item.z, head = item_head(item);
                 const int n_kv = (seg_len + BN - 1) / BN;
                 // Q pairs alternate between two buffers, so the next item's Q is loaded while
                 // the current item still runs
                 const uint32_t qb = q_it % C::QBUF, qn = q_it / C::QBUF;   // buffer, its use count
                 if (!q_early) {
                     if (qn > 0 && !(ok = wait(bars.q_empty[qb], (qn - 1) & 1))) break;
-                    load_q(qb, qn, q0, head);
+                    load_q(qb, qn, q0, head, item_split(item));
                 }
                 q_early = false;
-                const int it_next = it + (int)gridDim.x;
                 for (int j = 0; j < n_kv; ++j, ++g) {
                     if constexpr (FQ && C::QBUF == 2) {
                         if (!q_early && it_next < n_items) {
                             const uint32_t qb1 = (q_it + 1) & 1, qn1 = (q_it + 1) >> 1;
                             if (qn1 == 0 || mbar_test(bar_addr(bars.q_empty[qb1]), (qn1 - 1) & 1)) {
-                                const Item nx = items[it_next];
-                                load_q(qb1, qn1, nx.z, nx.w);
+                                load_q(qb1, qn1, nx.z, item_head(nx), item_split(nx));
                                 q_early = true;
                             }
                         }
@@ -254,7 +301,10 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                     head * D + 16 * s, row, bar_addr(bars.v_full[st]));
                     v_pend = (v_pend & ~(3u << (2 * st))) | ((((g / ST) & 1) + 1) << (2 * st));
                 }
+                it = it_next;
+                item = nx;
             }
+            if (ok) publish(kEnd);                           // the other roles stop at this entry
             if (!ok) {
                 // let every copy already issued land before this CTA's shared memory is released
                 // (loads that completed earlier return at once; short budget, abort flag ignored)
@@ -290,12 +340,15 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint32_t tS = tmem + (ti ? C::TS1 : C::TS0);
             const uint32_t tO = tmem + (ti ? C::TO1 : C::TO0);
             const uint32_t tP = tmem + (ti ? C::TP1 : C::TP0);
-            const uint64_t dq_base = smem_desc(smem_addr(base + C::OFF_Q + ti * C::Q_TILE), 16, 256, 6);
+            const uint64_t dq_own = smem_desc(smem_addr(base + C::OFF_Q + ti * C::Q_TILE), 16, 256, 6);
+            const uint64_t dq_tile0 = smem_desc(smem_addr(base + C::OFF_Q), 16, 256, 6);
             const uint64_t dk0 = smem_desc(smem_addr(base + C::OFF_K), 16, 256, 6);
             const uint64_t dv0 = smem_desc(smem_addr(base + C::OFF_V), C::KV_SLAB, 256, 6);
             const uint64_t &b_sfree = bars.s_free[ti], &b_pfull = bars.p_full[ti], &b_ofree = bars.o_free[ti];
             const uint32_t a_sfull = bar_addr(bars.s_full[ti]), a_pvdone = bar_addr(bars.pv_done[ti]);
-            uint32_t t = 0, item_cnt = 0;             // global key-tile counter, items done
+            // t: key tiles this CTA has passed through the K/V ring (every one, own or not: stage
+            // and phase of each); c: S tiles this issuer has computed (parity of s_free, p_full)
+            uint32_t t = 0, c = 0, item_cnt = 0;
             bool ok = true;
 
             auto qk = [&](uint64_t dq, uint64_t dk) {
@@ -312,51 +365,116 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 mma_commit(a_pvdone);
             };
 
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_cnt) {
-                const Item item = items[it];
+            for (Item item; take_item(item_cnt, item, false, ok); ++item_cnt) {
                 const int n_kv = (item.y + BN - 1) / BN;
                 const int n_full = item.y / BN;                  // tiles with BN keys of the segment
                 uint32_t st = t % ST, ph = (t / ST) & 1;
                 const uint32_t qb = item_cnt % C::QBUF;         // Q buffer of this item
-                const uint64_t dq = dq_base + qb * ((2 * C::Q_TILE) >> 4);
                 if (!(ok = wait(FQ ? bars.q_ready[qb] : bars.q_full[qb], (item_cnt / C::QBUF) & 1))) break;
-                // prologue: S of the item's first key tile
-                if (!(ok = wait(bars.k_full[st], ph))) break;
-                if (t > 0 && !(ok = wait(b_sfree, (t - 1) & 1))) break;
-                tc_fence_after();
-                qk(dq, dk0 + st * STAGE_STEP);
-                if (n_kv == 1) mma_commit(bar_addr(bars.q_empty[qb]));
-                // one key tile: QK of the next tile, then P.V of this one; the tail variant (the last
-                // tile of a segment that ends inside it) is a separate copy after the loop, so the
-                // loop over full tiles carries no test for it
-                auto step = [&](int j, auto tail) -> bool {
-                    const uint32_t u = t + j;                 // global index of this key tile
-                    const uint32_t st1 = (st + 1 == (uint32_t)ST) ? 0u : st + 1;
-                    const uint32_t ph1 = (st + 1 == (uint32_t)ST) ? ph ^ 1u : ph;
-                    if (j + 1 < n_kv) {                        // next tile's S as soon as this S was read
-                        if (!(ok = wait(bars.k_full[st1], ph1))) return false;
-                        if (!(ok = wait(b_sfree, u & 1))) return false;
-                        tc_fence_after();
-                        qk(dq, dk0 + st1 * STAGE_STEP);
-                        if (j + 2 == n_kv) mma_commit(bar_addr(bars.q_empty[qb]));
-                    }
-                    if (!(ok = wait(bars.v_full[st], ph))) return false;
-                    if (j == 0 && item_cnt > 0 && !(ok = wait(b_ofree, (item_cnt - 1) & 1))) return false;
-                    if (!(ok = wait(b_pfull, u & 1))) return false;
+                if (!item_split(item)) {
+                    const uint64_t dq = dq_own + qb * ((2 * C::Q_TILE) >> 4);
+                    // prologue: S of the item's first key tile
+                    if (!(ok = wait(bars.k_full[st], ph))) break;
+                    if (c > 0 && !(ok = wait(b_sfree, (c - 1) & 1))) break;
                     tc_fence_after();
-                    if constexpr (decltype(tail)::value)
-                        pv_tail<NSLAB, C::KV_SLAB, D>(tO, tP, dv0 + st * STAGE_STEP, base + C::OFF_V + st * C::KV_TILE,
-                                                      j > 0 ? 1u : 0u, item.y - j * BN, a_pvdone);
+                    qk(dq, dk0 + st * STAGE_STEP);
+                    if (n_kv == 1) mma_commit(bar_addr(bars.q_empty[qb]));
+                    // one key tile: QK of the next tile, then P.V of this one; the tail variant (the
+                    // last tile of a segment that ends inside it) is a separate copy after the loop,
+                    // so the loop over full tiles carries no test for it
+                    auto step = [&](int j, auto tail) -> bool {
+                        const uint32_t u = c + j;                 // this issuer's S count of this tile
+                        const uint32_t st1 = (st + 1 == (uint32_t)ST) ? 0u : st + 1;
+                        const uint32_t ph1 = (st + 1 == (uint32_t)ST) ? ph ^ 1u : ph;
+                        if (j + 1 < n_kv) {                        // next tile's S as soon as this S was read
+                            if (!(ok = wait(bars.k_full[st1], ph1))) return false;
+                            if (!(ok = wait(b_sfree, u & 1))) return false;
+                            tc_fence_after();
+                            qk(dq, dk0 + st1 * STAGE_STEP);
+                            if (j + 2 == n_kv) mma_commit(bar_addr(bars.q_empty[qb]));
+                        }
+                        if (!(ok = wait(bars.v_full[st], ph))) return false;
+                        if (j == 0 && item_cnt > 0 && !(ok = wait(b_ofree, (item_cnt - 1) & 1))) return false;
+                        if (!(ok = wait(b_pfull, u & 1))) return false;
+                        tc_fence_after();
+                        if constexpr (decltype(tail)::value)
+                            pv_tail<NSLAB, C::KV_SLAB, D>(tO, tP, dv0 + st * STAGE_STEP,
+                                                          base + C::OFF_V + st * C::KV_TILE, j > 0 ? 1u : 0u,
+                                                          item.y - j * BN, a_pvdone);
+                        else
+                            pv(dv0 + st * STAGE_STEP, j > 0 ? 1u : 0u);
+                        mma_commit(bar_addr(bars.kv_empty[st]));
+                        st = st1;
+                        ph = ph1;
+                        return true;
+                    };
+                    for (int j = 0; j < n_full; ++j)
+                        if (!step(j, std::false_type{})) break;
+                    if (ok && n_full < n_kv) step(n_full, std::true_type{});
+                    t += n_kv;
+                    c += n_kv;
+                    continue;
+                }
+                // Split item: one Q tile (tile 0 of the buffer), this issuer takes the key tiles
+                // j = ti, ti + 2, ...; it still waits for the K and V of every tile as they pass, so
+                // that each of its parity waits is at most one phase ahead of its barrier. A tile's
+                // only consumer commits its kv_empty twice (the barrier expects two arrivals).
+                const uint64_t dq = dq_tile0 + qb * ((2 * C::Q_TILE) >> 4);
+                int prev_j = -1;                                  // own tile whose P.V is pending
+                uint32_t prev_st = 0, prev_ph = 0, prev_c = 0;
+                bool first_pv = true;
+                auto pv_of_prev = [&]() -> bool {
+                    if (!(ok = wait(bars.v_full[prev_st], prev_ph))) return false;
+                    if (first_pv && item_cnt > 0 && !(ok = wait(b_ofree, (item_cnt - 1) & 1))) return false;
+                    if (!(ok = wait(b_pfull, prev_c & 1))) return false;
+                    tc_fence_after();
+                    const uint32_t acc = first_pv ? 0u : 1u;
+                    if (prev_j < n_full)
+                        pv(dv0 + prev_st * STAGE_STEP, acc);
                     else
-                        pv(dv0 + st * STAGE_STEP, j > 0 ? 1u : 0u);
-                    mma_commit(bar_addr(bars.kv_empty[st]));
-                    st = st1;
-                    ph = ph1;
+                        pv_tail<NSLAB, C::KV_SLAB, D>(tO, tP, dv0 + prev_st * STAGE_STEP,
+                                                      base + C::OFF_V + prev_st * C::KV_TILE, acc,
+                                                      item.y - prev_j * BN, a_pvdone);
+                    mma_commit(bar_addr(bars.kv_empty[prev_st]));
+                    mma_commit(bar_addr(bars.kv_empty[prev_st]));
+                    first_pv = false;
                     return true;
                 };
-                for (int j = 0; j < n_full; ++j)
-                    if (!step(j, std::false_type{})) break;
-                if (ok && n_full < n_kv) step(n_full, std::true_type{});
+                // With three ring slots the next own tile's QK goes out before the pending P.V, as in
+                // the two-tile path; with two, the pending tile's slot must be released first, since
+                // the next own tile's K is loaded into it.
+                constexpr bool qk_first = ST >= 3;
+                for (int j = 0; j < n_kv; ++j) {
+                    if ((j & 1) != ti) {
+                        if (!(ok = wait(bars.k_full[st], ph))) break;
+                        if (!(ok = wait(bars.v_full[st], ph))) break;
+                    } else {
+                        if (!qk_first && prev_j >= 0 && !pv_of_prev()) break;
+                        if (!(ok = wait(bars.k_full[st], ph))) break;
+                        if (c > 0 && !(ok = wait(b_sfree, (c - 1) & 1))) break;
+                        tc_fence_after();
+                        qk(dq, dk0 + st * STAGE_STEP);
+                        if (j + 2 >= n_kv) mma_commit(bar_addr(bars.q_empty[qb]));   // last own QK
+                        if (qk_first && prev_j >= 0 && !pv_of_prev()) break;
+                        prev_j = j;
+                        prev_st = st;
+                        prev_ph = ph;
+                        prev_c = c++;
+                    }
+                    if (++st == (uint32_t)ST) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (prev_j >= 0) {
+                    if (!pv_of_prev()) break;
+                } else {
+                    // no key tile of this item is this issuer's (a single-tile segment): release the
+                    // Q buffer, and keep o_free's phase count in step with the items
+                    mbar_arrive(bar_addr(bars.q_empty[qb]));
+                    if (item_cnt > 0 && !(ok = wait(b_ofree, (item_cnt - 1) & 1))) break;
+                }
                 t += n_kv;
             }
             // drain: nothing this thread issued may still be running when TMEM is freed
@@ -372,14 +490,14 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // belong to no result and are left as loaded.
             uint32_t item_cnt = 0;
             bool ok = true;
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_cnt) {
-                const Item item = items[it];
+            for (Item item; take_item(item_cnt, item, true, ok); ++item_cnt) {
                 const int64_t seg_end = (int64_t)item.x + item.y, q0 = item.z;
                 const uint32_t qb = item_cnt % C::QBUF;
                 if (!(ok = wait_warp(bars.q_full[qb], (item_cnt / C::QBUF) & 1))) break;
                 unsigned char *qbuf = base + C::OFF_Q + 2 * qb * C::Q_TILE;
+                const int n_rows = item_split(item) ? BM : 2 * BM;   // a split item has one Q tile
 #pragma unroll 1
-                for (int k = 0; k < 2 * BM / 32; ++k) {
+                for (int k = 0; k < n_rows / 32; ++k) {
                     const int row = lane + 32 * k;
                     if (q0 + row >= seg_end) continue;
                     const int r = row % BM;
@@ -393,6 +511,12 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_addr(bars.q_ready[qb]));
             }
+        } else if (lane == 0) {
+            // nothing to do but free its share of every item ring slot
+            bool ok = true;
+            Item item;
+            for (uint32_t k = 0; take_item(k, item, false, ok); ++k) {
+            }
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax groups
@@ -404,17 +528,19 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t tS = t_lane + (grp ? C::TS1 : C::TS0);
         const uint32_t tO = t_lane + (grp ? C::TO1 : C::TO0);
         const uint32_t tP = t_lane + (grp ? C::TP1 : C::TP0);
-        uint32_t s_cnt = 0, p_cnt = 0, item_cnt = 0;
+        // P tiles this group has written; at the top of the tile loop it also counts the S tiles read
+        uint32_t p_cnt = 0, item_cnt = 0;
         bool ok = true;
 
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_cnt) {
-            const Item item = items[it];
-            const int seg0 = item.x, seg_len = item.y, q0 = item.z, head = item.w;
+        for (Item item; take_item(item_cnt, item, true, ok); ++item_cnt) {
+            const int seg0 = item.x, seg_len = item.y, q0 = item.z, head = item_head(item);
             const int n_kv = (seg_len + BN - 1) / BN;
+            // own key tiles: every one, or in a split item every other one starting at this group's
+            const int dj = item_split(item) ? 2 : 1;
             float m_run = -INFINITY, l_run = 0.f;
 
-            for (int j = 0; j < n_kv && ok; ++j) {
-                if (!(ok = wait_warp(bars.s_full[grp], s_cnt & 1))) break;
+            for (int j = dj == 2 ? grp : 0; j < n_kv && ok; j += dj) {
+                if (!(ok = wait_warp(bars.s_full[grp], p_cnt & 1))) break;
                 tc_fence_after();
                 // S row -> registers: all loads in flight, one wait
                 uint32_t sr[BN];
@@ -425,7 +551,6 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_addr(bars.s_free[grp]));
-                ++s_cnt;
 
                 // the previous P.V of this tile has almost always finished by now: probe it
                 // without blocking, so its barrier latency overlaps the arithmetic below
@@ -453,7 +578,8 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     alpha = ex2(m_run - m_tile);
                     m_run = m_tile;
                 }
-                const bool rescale = (j > 0) && (alpha != 1.f);
+                // the first own tile of an item (l_run still 0) overwrites O: its P.V does not accumulate
+                const bool rescale = (l_run != 0.f) && (alpha != 1.f);
                 // p = exp2(s * scale*log2(e) - m): pairs through the f32x2 FMA, row sum in f32x2 adds
                 uint32_t pk[BN / 2];
                 const uint64_t sc2 = f2_splat(scale_log2), nm2 = f2_splat(-m_run);
@@ -499,33 +625,97 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             if (!ok) break;
 
-            // epilogue: wait for this tile's last P.V, then O / l -> bf16 -> HBM
-            if (!(ok = wait_warp(bars.pv_done[grp], (p_cnt - 1) & 1))) break;
-            tc_fence_after();
-            const int q_row = q0 + grp * BM + row;
-            const bool store = q_row < seg0 + seg_len;
-            const float inv_l = 1.f / l_run;
-            // l_run sums exp2(s * scale*log2(e) - m_run), so ln(sum exp(scale * s)) = (m_run + log2 l_run) ln 2
-            if (LSE && store) lse[(int64_t)q_row * H + head] = (m_run + log2f(l_run)) * 0.6931471805599453f;
-            __nv_bfloat16 *dst = out + (int64_t)q_row * out_stride + (int64_t)head * D;
+            if (dj == 1) {
+                // epilogue: wait for this tile's last P.V, then O / l -> bf16 -> HBM
+                if (!(ok = wait_warp(bars.pv_done[grp], (p_cnt - 1) & 1))) break;
+                tc_fence_after();
+                const int q_row = q0 + grp * BM + row;
+                const bool store = q_row < seg0 + seg_len;
+                const float inv_l = 1.f / l_run;
+                // l_run sums exp2(s * scale*log2(e) - m_run), so ln(sum exp(scale * s)) = (m_run + log2 l_run) ln 2
+                if (LSE && store) lse[(int64_t)q_row * H + head] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+                __nv_bfloat16 *dst = out + (int64_t)q_row * out_stride + (int64_t)head * D;
 #pragma unroll
-            for (int c = 0; c < D; c += 16) {
-                uint32_t r[16];
-                tmem_ld16(tO + c, r);
-                tmem_wait_ld();
-                reg_fence(r);
-                uint32_t o[8];
+                for (int c = 0; c < D; c += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tO + c, r);
+                    tmem_wait_ld();
+                    reg_fence(r);
+                    uint32_t o[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    o[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-                if (store) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
-                    d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                    d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    for (int e = 0; e < 8; ++e)
+                        o[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+                    if (store) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+                        d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_addr(bars.o_free[grp]));
+                continue;
+            }
+
+            // split item: the two groups hold partial results of the same 128 rows over disjoint
+            // key tiles (group g: O_g, running max m_g, row sum l_g, all relative to m_g). Each
+            // group waits for its last P.V, publishes (m_g, l_g), and after the first meeting
+            // writes half of the head's columns of
+            //   out = (2^(m_0 - M) O_0 + 2^(m_1 - M) O_1) / (2^(m_0 - M) l_0 + 2^(m_1 - M) l_1),
+            // M = max(m_0, m_1), reading both groups' O. A group with no tile of this item (a
+            // one-tile segment) contributes nothing: its O is never read. The second meeting
+            // keeps either O region from being overwritten before both groups have read it.
+            const int n_own1 = n_kv >> 1;                     // key tiles of group 1 (group 0 has >= 1)
+            const bool mine = grp ? n_own1 > 0 : true;
+            if (mine && !(ok = wait_warp(bars.pv_done[grp], (p_cnt - 1) & 1))) break;
+            s_m[grp][row] = m_run;
+            s_l[grp][row] = l_run;
+            tc_fence_before();
+            __syncwarp();
+            // every split item takes the merge barrier through two phases: parity 0, then 1
+            if (lane == 0) mbar_arrive(bar_addr(bars.merge));
+            if (!(ok = wait_warp(bars.merge, 0))) break;
+            tc_fence_after();
+            // this group's (m, l) are still in registers; the other group's come from shared memory
+            const float m_oth = s_m[grp ^ 1][row], l_oth = s_l[grp ^ 1][row];
+            const bool oth_has = grp ? true : n_own1 > 0;     // group 0 always has a tile
+            const float M = oth_has ? fmaxf(m_run, m_oth) : m_run;
+            const float w_own = mine ? ex2(m_run - M) : 0.f, w_oth = oth_has ? ex2(m_oth - M) : 0.f;
+            const float l_sum = w_own * l_run + w_oth * l_oth;
+            const float inv_l = 1.f / l_sum;
+            const float c0 = (grp ? w_oth : w_own) * inv_l, c1 = (grp ? w_own : w_oth) * inv_l;
+            const int q_row = q0 + row;
+            const bool store = q_row < seg0 + seg_len;
+            if (LSE && store && grp == 0) lse[(int64_t)q_row * H + head] = (M + log2f(l_sum)) * 0.6931471805599453f;
+            constexpr int HALF = D / 2;                        // columns of the head this group writes
+            static_assert(HALF % 8 == 0, "each group writes whole 16-byte pieces");
+            static_assert(C::TO1 == C::TO0 + D, "O1 follows O0");
+            const uint32_t tO0 = tO - grp * HALF, tO1 = tO0 + D;     // this group's columns of O0 and O1
+            __nv_bfloat16 *dst = out + (int64_t)q_row * out_stride + (int64_t)head * D + grp * HALF;
+#pragma unroll
+            for (int c = 0; c < HALF; c += 8) {
+                uint32_t r0[8], r1[8];
+                tmem_ld8(tO0 + c, r0);
+                if (n_own1 > 0) tmem_ld8(tO1 + c, r1);
+                tmem_wait_ld();
+                reg_fence(r0);
+                if (n_own1 > 0) reg_fence(r1);
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float x0 = __uint_as_float(r0[2 * e]) * c0, x1 = __uint_as_float(r0[2 * e + 1]) * c0;
+                    if (n_own1 > 0) {
+                        x0 = fmaf(__uint_as_float(r1[2 * e]), c1, x0);
+                        x1 = fmaf(__uint_as_float(r1[2 * e + 1]), c1, x1);
+                    }
+                    o[e] = pack_bf16x2(x0, x1);
+                }
+                if (store) *reinterpret_cast<uint4 *>(dst + c) = make_uint4(o[0], o[1], o[2], o[3]);
             }
             tc_fence_before();
             __syncwarp();
+            if (lane == 0) mbar_arrive(bar_addr(bars.merge));
+            if (!(ok = wait_warp(bars.merge, 1))) break;
             if (lane == 0) mbar_arrive(bar_addr(bars.o_free[grp]));
         }
     }
@@ -595,7 +785,8 @@ cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, int stal
     if (blocks == 0) return cudaSuccess;
     LaunchScope scope("attn_long", stream);
     kern<<<blocks, kThreads, C::SMEM, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16 *>(a.out),
-                                                               a.out_stride, a.lse, a.H, a.scale_log2, a.hdr,
+                                                               a.out_stride, a.lse, a.H, a.scale_log2,
+                                                               const_cast<WsHeader *>(a.hdr),
                                                                a.items, a.status, stall_v, a.qr);
     return cudaGetLastError();
 }

@@ -24,7 +24,7 @@
 // Any segment length works (longer ones loop over 128-key tiles). With the
 // default split it has no work: segments of at most 64 tokens go to the
 // tiny-segment kernel and longer ones to the tcgen05 kernel; it takes the band
-// between 64 tokens and a caller-raised split (vit_set_short_segment_max).
+// between 64 tokens and a split a caller raises through vit_varlen_attn_ex.
 #include "internal.h"
 #include "warp_mma.cuh"
 

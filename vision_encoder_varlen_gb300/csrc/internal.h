@@ -14,8 +14,16 @@ namespace vit {
 
 // Work item of the attention kernels: one (segment, head, q-block).
 //   x = first token of the segment, y = segment length,
-//   z = first query token of the block, w = head.
+//   z = first query token of the block, w = head | kItemSplit when set.
+// A long-segment item covers 256 query rows as two 128-row Q tiles that share every key tile;
+// with kItemSplit it covers 128 rows, and its two halves of the long kernel take alternate key
+// tiles of the segment and merge their partial results at the end (used for a segment's last
+// block of at most 128 rows, and for every block when a batch has too few items to fill the GPU).
 using Item = int4;
+constexpr int kItemSplit = 1 << 30;
+constexpr int kMaxHeads = 1 << 24;            // heads fit below the flag bit
+__host__ __device__ inline int item_head(const Item &it) { return it.w & (kItemSplit - 1); }
+__host__ __device__ inline bool item_split(const Item &it) { return (it.w & kItemSplit) != 0; }
 
 // Header at the start of the attention workspace, written by the scheduler.
 struct WsHeader {
@@ -25,7 +33,9 @@ struct WsHeader {
     int32_t bm_short;    // query rows per short (and tiny) item
     int32_t error;       // device-detected error of the last scheduling pass (0 = none)
     int32_t n_tiny;      // items [n_long + n_short, + n_tiny) go to the tiny-segment kernel
-    int32_t pad[10];
+    int32_t long_all_split;   // 1 when every long item is a split item of bm_long / 2 rows
+    int32_t next_long;   // long items handed out so far beyond each CTA's first (zeroed by the scheduler)
+    int32_t pad[8];
 };
 static_assert(sizeof(WsHeader) == 64, "header is 64 bytes");
 
@@ -35,6 +45,8 @@ struct SchedParams {
     int tiny_max;    // of those, segments with length <= tiny_max use the tiny-segment kernel
     int bm_long;     // q rows per long item
     int bm_short;    // q rows per short item (a tiny segment is always one item per head)
+    int num_sms;     // SMs of the device: with at most num_sms / 2 long items of bm_long rows, every
+                     // long block is cut to bm_long / 2 rows and split over its key tiles instead
 };
 
 // Upper bound on the number of items of one class for these sizes.
@@ -116,5 +128,17 @@ cudaError_t launch_attn_tiny(const AttnArgs &a, int64_t max_items_tiny, int num_
 
 cudaError_t launch_attn_long(const AttnArgs &a, int64_t max_items_long, int num_sms, int stall_v,
                              cudaStream_t stream);
+
+// Every host-side check of the attention calls except those of the workspace (api.cu).
+// *nothing is set when the call has no work at all (no segments, no tokens).
+vit_status_t check_varlen_attn_args(const void *q, const void *k, const void *v, int64_t T, int H, int D,
+                                    int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                                    const vit_q_rope_t *q_rope, const int32_t *cu_seqlens, const int32_t *seq_start,
+                                    const int32_t *seq_len, int B, int max_seqlen, float scale, const void *out,
+                                    int64_t out_stride, const float *lse, const vit_attn_options_t *opts,
+                                    bool *nothing);
+
+// VIT_OK when the current device is one this library was built for.
+vit_status_t check_device();
 
 }  // namespace vit

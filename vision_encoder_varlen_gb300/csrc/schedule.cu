@@ -17,7 +17,10 @@
 //      their items are small, so sorting them buys no balance and cost most of
 //      the scheduler's time for thousands of small images);
 //   3. expands every segment into (segment, head, q-block) work items: long
-//      segments into blocks of bm_long query rows for the long-segment kernel,
+//      segments into blocks of bm_long query rows for the long-segment kernel
+//      (a last block of at most bm_long / 2 rows, and every block of a batch
+//      too small to give each SM two blocks' worth of items, as a split item
+//      of bm_long / 2 rows whose two halves take alternate key tiles),
 //      short ones into blocks of bm_short rows for the short-segment kernel,
 //      tiny ones (at most tiny_max tokens) into one item per head for the
 //      tiny-segment kernel. Longest first, the three classes come out as three
@@ -111,6 +114,8 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
             hdr->n_long = 0;
             hdr->n_short = 0;
             hdr->n_tiny = 0;
+            hdr->long_all_split = 0;
+            hdr->next_long = 0;
             hdr->error = s_err == 1 ? VIT_ERR_BAD_SEQLENS : VIT_ERR_SEQLEN_EXCEEDS_MAX;
             report_error(status, hdr->error);
         }
@@ -162,7 +167,18 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
     // ---- 3. item counts per position, exclusive scan, expansion
     // (the block sizes are powers of two: shifts instead of divisions, which otherwise dominate
     // this single block's instruction count for thousands of segments)
-    const int lg_long = __ffs(sp.bm_long) - 1, lg_short = __ffs(sp.bm_short) - 1;
+    // Long blocks are bm_long rows (two Q tiles) unless the whole batch would give at most
+    // num_sms / 2 of them: then every long block is cut to bm_long / 2 rows, twice as many items,
+    // each split over its key tiles, so twice as many SMs work on the batch.
+    const int lg_full = __ffs(sp.bm_long) - 1, lg_short = __ffs(sp.bm_short) - 1;
+    int64_t local_full = 0, total_full;
+    for (int p = lo; p < hi; ++p) {
+        const int len = s_len[s_order[p]];
+        if (len > sp.short_max) local_full += (int64_t)H * ((len + (1 << lg_full) - 1) >> lg_full);
+    }
+    block_exclusive_scan(local_full, s_warp, &total_full);
+    const bool all_split = 2 * total_full <= (int64_t)sp.num_sms;
+    const int lg_long = all_split ? lg_full - 1 : lg_full;
     auto n_blocks = [&](int len) {
         const int lg = len > sp.short_max ? lg_long : lg_short;
         return (len + (1 << lg) - 1) >> lg;
@@ -192,16 +208,22 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
         const int seg = s_order[p];
         const int len = s_len[seg];
         if (len == 0) continue;
-        const int bm = len > sp.short_max ? sp.bm_long : sp.bm_short;
+        const bool is_long = len > sp.short_max;
+        const int bm = is_long ? (1 << lg_long) : sp.bm_short;
         const int nq = n_blocks(len);
         const int start = s_start[seg];
+        // a long item is split when every long item is, or when it is the segment's last block
+        // and holds at most bm_long / 2 rows (its second Q tile would be empty)
+        const int last_rows = len - (nq - 1) * bm;
+        const int split_last = is_long && (all_split || 2 * last_rows <= sp.bm_long) ? kItemSplit : 0;
+        const int split_rest = is_long && all_split ? kItemSplit : 0;
         Item *dst = items + s_off[p];
         if (nq == 1) {                                     // one query block: item i is head i
-            for (int i = lane; i < H; i += 32) dst[i] = make_int4(start, len, start, i);
+            for (int i = lane; i < H; i += 32) dst[i] = make_int4(start, len, start, i | split_last);
         } else {
             for (int i = lane; i < H * nq; i += 32) {
                 const int h = i / nq, qb = i - h * nq;
-                dst[i] = make_int4(start, len, start + qb * bm, h);
+                dst[i] = make_int4(start, len, start + qb * bm, h | (qb == nq - 1 ? split_last : split_rest));
             }
         }
     }
@@ -209,9 +231,11 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
         hdr->n_long = (int32_t)total_long;
         hdr->n_short = (int32_t)(total - total_long - total_tiny);
         hdr->n_tiny = (int32_t)total_tiny;
-        hdr->bm_long = sp.bm_long;
+        hdr->bm_long = 1 << lg_long;
         hdr->bm_short = sp.bm_short;
         hdr->error = 0;
+        hdr->long_all_split = all_split ? 1 : 0;
+        hdr->next_long = 0;
     }
 }
 
