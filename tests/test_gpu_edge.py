@@ -199,52 +199,56 @@ def test_launches_are_counted_and_timed():
     assert "schedule" in rec and all(ms >= 0 for _, ms in rec.values())
 
 
-def _test_hooks_library():
-    """The library rebuilt with its failure-path test hook (never shipped): the release library
-    exports no debug call."""
-    import ctypes
-    L = ctypes.CDLL(_build.build_test_hooks())
-    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
-    L.vit_debug_stall_long_kernel.argtypes = [i32]
-    L.vit_debug_stall_long_kernel.restype = i32
-    L.vit_varlen_attn_ex.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, i64, vp, vp, vp, i32, i32, f32, vp, i64,
-                                     vp, vp, ctypes.POINTER(vit._AttnOptions), vp, sz, vp, vp]
-    L.vit_varlen_attn_ex.restype = i32
-    return L
+_STALL_SCRIPT = """
+import ctypes, json, sys
+import numpy as np
+import torch
+sys.path[:0] = [{root!r}, {tests!r}]
+import oracle
+import vision_encoder_varlen_gb300 as vit
+from vision_encoder_varlen_gb300 import workloads as wl
+from helpers import assert_close
+vit.LIB_PATH = {lib!r}                 # this process loads the test build only
+L = vit.lib()
+L.vit_debug_stall_long_kernel.argtypes = [ctypes.c_int]
+L.vit_debug_stall_long_kernel.restype = ctypes.c_int
+w = wl.from_lengths([600, 300], 2, 80, seed=wl.SEED_BASE + 7, max_seqlen_meta=131072)
+t = w.tensors()
+q, k, v = (t[n].cuda() for n in ("q", "k", "v"))
+cu = torch.from_numpy(w.cu_seqlens).cuda()
+vit.varlen_attn(q, k, v, cu, w.max_seqlen, short_max=0)      # every kernel loaded before the stall
+torch.cuda.synchronize()
+status = vit.new_status()
+L.vit_debug_stall_long_kernel(1)
+try:
+    vit.varlen_attn(q, k, v, cu, w.max_seqlen, status=status, short_max=0)
+    code = vit.read_status(status)
+finally:
+    L.vit_debug_stall_long_kernel(0)
+status2 = vit.new_status()
+out = vit.varlen_attn(q, k, v, cu, w.max_seqlen, status=status2, short_max=0)
+code2 = vit.read_status(status2)
+ref = oracle.attention(*(oracle.widen(wl.bf16_bits(t[n])) for n in ("q", "k", "v")), w.cu_seqlens)
+mx, mean = assert_close(out, ref, what="after timeout")
+print("RESULT " + json.dumps([code, code2, mx]))
+"""
 
 
 def test_long_kernel_bounded_wait_reports_timeout_and_context_survives():
-    """A wait that can never complete (V is never loaded) must end in
-    VIT_ERR_TIMEOUT within its clock budget; afterwards the same process
-    computes correct results again."""
-    import ctypes
-    w, t, cu, (q, k, v) = _inputs([600, 300], 2, 80, seed=7)
-    L = _test_hooks_library()
-    T, H, D = q.shape
-    out = torch.empty_like(q)
-    ws = torch.empty(vit.workspace_size(T, H, w.num_segments, D), dtype=torch.uint8, device="cuda")
-    opts = vit._AttnOptions(0)                     # every segment on the tcgen05 kernel
-    p = lambda x: ctypes.c_void_p(x.data_ptr())
-
-    def call(status):
-        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-        return L.vit_varlen_attn_ex(p(q), p(k), p(v), T, H, D, q.stride(0), k.stride(0), v.stride(0), p(cu), None,
-                                    None, w.num_segments, w.max_seqlen, 0.0, p(out), out.stride(0), None, None,
-                                    ctypes.byref(opts), p(ws), ws.numel(), p(status), stream)
-
-    status = vit.new_status()
-    L.vit_debug_stall_long_kernel(1)
-    try:
-        assert call(status) == 0
-        code = vit.read_status(status)
-    finally:
-        L.vit_debug_stall_long_kernel(0)
-    assert code == -13
-    status2 = vit.new_status()
-    assert call(status2) == 0
-    assert vit.read_status(status2) == 0
-    ref = oracle.attention(*(oracle.widen(wl.bf16_bits(t[n])) for n in ("q", "k", "v")), w.cu_seqlens)
-    assert_close(out, ref, what="after timeout")
+    """A wait that can never complete (V is never loaded) must end in VIT_ERR_TIMEOUT within its
+    clock budget; afterwards the same process computes correct results again. The hook exists
+    only in a test build of the library (the release library exports no debug call), which a
+    separate process loads alone; a first call there loads every kernel the stalled call uses."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = _STALL_SCRIPT.format(root=root, tests=os.path.join(root, "tests"), lib=_build.build_test_hooks())
+    r = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True, timeout=240)
+    assert r.returncode == 0, r.stderr[-3000:]
+    line = [x for x in r.stdout.splitlines() if x.startswith("RESULT ")][-1]
+    code, code2, _ = __import__("json").loads(line[len("RESULT "):])
+    assert code == -13 and code2 == 0
 
 
 def test_threads_with_different_splits_get_their_own_results():

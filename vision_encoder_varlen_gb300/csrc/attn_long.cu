@@ -64,6 +64,7 @@ constexpr int kSoftmaxRegs = 208;             // softmax warpgroups after setmax
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split exceeds the launch pool");
 constexpr int BM = 128;                       // rows per Q tile; two tiles per item
 constexpr long long kWaitBudget = 4000000000ll;   // clock cycles before a wait gives up (~2 s)
+constexpr int kMaxStages = 4;                 // K/V ring slots the barrier arrays hold
 constexpr int kItemRing = 4;                  // items the producer may publish ahead of the other roles
 constexpr int kItemReaders = 11;              // the two issuers, warp 3 and the eight softmax warps
 
@@ -95,12 +96,13 @@ template <int D> struct LongCfg {
     static constexpr int TP1 = (TP0 + BN / 2 + 7) / 8 * 8;
     static_assert(TP1 + BN / 2 <= 512, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory per block (227 KB opt-in limit)");
+    static_assert(STAGES >= 2 && STAGES <= kMaxStages, "ring slots the barrier arrays hold");
     static_assert(D % 16 == 0 && BN % 16 == 0 && (BN / 2) % 8 == 0, "tile shapes");
 };
 
 struct Bars {
     uint64_t q_full[2], q_empty[2], q_ready[2];
-    uint64_t k_full[3], v_full[3], kv_empty[3];
+    uint64_t k_full[kMaxStages], v_full[kMaxStages], k_empty[kMaxStages], v_empty[kMaxStages];
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
     uint64_t drain[2];
     uint64_t merge;          // split items: the eight softmax warps meet twice at the item's end
@@ -166,7 +168,8 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int s = 0; s < ST; ++s) {
             mbar_init(bar_addr(bars.k_full[s]), 1);
             mbar_init(bar_addr(bars.v_full[s]), 1);
-            mbar_init(bar_addr(bars.kv_empty[s]), 2);    // one commit from each MMA issuer
+            mbar_init(bar_addr(bars.k_empty[s]), 2);     // one commit from each MMA issuer after its QK
+            mbar_init(bar_addr(bars.v_empty[s]), 2);     // and after its P.V
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(bars.s_full[i]), 1);
@@ -243,6 +246,23 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                     head * D + 16 * s, q0 + BM * i, bar_addr(bars.q_full[qb]));
                 q_pend = (q_pend & ~(3u << (2 * qb))) | (((qn & 1) + 1) << (2 * qb));
             };
+            // K and V of a tile go into separate halves of a ring slot: a slot's K half is free once
+            // its QK has completed, its V half only once its P.V has. So each tile's V is issued
+            // after the next tile's K: that K load waits on an earlier event than this V load would,
+            // and the K of the tile after next reaches shared memory well before its QK.
+            uint32_t v_g = 0;                                // pending V: ring index, first row, head
+            int v_row = -1, v_head = 0;
+            auto load_v = [&]() -> bool {
+                const int st = v_g % ST;
+                if (v_g >= (uint32_t)ST && !(ok = wait(bars.v_empty[st], (v_g / ST - 1) & 1))) return false;
+                if (stall_v) return true;       // test hook: V never arrives, the MMA wait expires
+                mbar_arrive_expect_tx(bar_addr(bars.v_full[st]), C::KV_TILE);
+                for (int s = 0; s < NSLAB; ++s)
+                    tma_load_2d(smem_addr(base + C::OFF_V + st * C::KV_TILE + s * C::KV_SLAB), &tm_v,
+                                v_head * D + 16 * s, v_row, bar_addr(bars.v_full[st]));
+                v_pend = (v_pend & ~(3u << (2 * st))) | ((((v_g / ST) & 1) + 1) << (2 * st));
+                return true;
+            };
             // raw Q needs time for warp 3 to rotate it, so with two Q buffers the next item's Q
             // goes out as soon as its buffer is free rather than after this item's last K/V tile
             bool q_early = false;                            // Q of item q_it already issued
@@ -287,23 +307,22 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         }
                     }
                     const int st = g % ST;
-                    if (g >= (uint32_t)ST && !(ok = wait(bars.kv_empty[st], (g / ST - 1) & 1))) break;
+                    if (g >= (uint32_t)ST && !(ok = wait(bars.k_empty[st], (g / ST - 1) & 1))) break;
                     const int row = seg0 + j * BN;
                     mbar_arrive_expect_tx(bar_addr(bars.k_full[st]), C::KV_TILE);
                     for (int s = 0; s < NSLAB; ++s)
                         tma_load_2d(smem_addr(base + C::OFF_K + st * C::KV_TILE + s * C::KV_SLAB), &tm_k,
                                     head * D + 16 * s, row, bar_addr(bars.k_full[st]));
                     k_pend = (k_pend & ~(3u << (2 * st))) | ((((g / ST) & 1) + 1) << (2 * st));
-                    if (stall_v) continue;          // test hook: V never arrives, the MMA wait expires
-                    mbar_arrive_expect_tx(bar_addr(bars.v_full[st]), C::KV_TILE);
-                    for (int s = 0; s < NSLAB; ++s)
-                        tma_load_2d(smem_addr(base + C::OFF_V + st * C::KV_TILE + s * C::KV_SLAB), &tm_v,
-                                    head * D + 16 * s, row, bar_addr(bars.v_full[st]));
-                    v_pend = (v_pend & ~(3u << (2 * st))) | ((((g / ST) & 1) + 1) << (2 * st));
+                    if (v_row >= 0 && !load_v()) break;
+                    v_g = g;
+                    v_row = row;
+                    v_head = head;
                 }
                 it = it_next;
                 item = nx;
             }
+            if (ok && v_row >= 0) load_v();                 // the last tile's V
             if (ok) publish(kEnd);                           // the other roles stop at this entry
             if (!ok) {
                 // let every copy already issued land before this CTA's shared memory is released
@@ -330,7 +349,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // per tile halves it. Descriptors are precomputed 64-bit bases plus compile-time offsets
         // (the address field is the low 14 bits and never carries); every barrier parity derives
         // from one global key-tile counter. The two issuers share nothing but the K/V stage
-        // barriers (two-arrival kv_empty / q_empty); each softmax group rewrites its tile's P
+        // barriers (two-arrival k_empty / v_empty / q_empty); each softmax group rewrites its tile's P
         // region only after that tile's previous P.V has completed.
         if (lane == 0) {
             const int ti = warp - 1;                              // Q tile of this issuer
@@ -378,6 +397,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (c > 0 && !(ok = wait(b_sfree, (c - 1) & 1))) break;
                     tc_fence_after();
                     qk(dq, dk0 + st * STAGE_STEP);
+                    mma_commit(bar_addr(bars.k_empty[st]));
                     if (n_kv == 1) mma_commit(bar_addr(bars.q_empty[qb]));
                     // one key tile: QK of the next tile, then P.V of this one; the tail variant (the
                     // last tile of a segment that ends inside it) is a separate copy after the loop,
@@ -391,6 +411,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             if (!(ok = wait(b_sfree, u & 1))) return false;
                             tc_fence_after();
                             qk(dq, dk0 + st1 * STAGE_STEP);
+                            mma_commit(bar_addr(bars.k_empty[st1]));
                             if (j + 2 == n_kv) mma_commit(bar_addr(bars.q_empty[qb]));
                         }
                         if (!(ok = wait(bars.v_full[st], ph))) return false;
@@ -403,7 +424,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                                           item.y - j * BN, a_pvdone);
                         else
                             pv(dv0 + st * STAGE_STEP, j > 0 ? 1u : 0u);
-                        mma_commit(bar_addr(bars.kv_empty[st]));
+                        mma_commit(bar_addr(bars.v_empty[st]));
                         st = st1;
                         ph = ph1;
                         return true;
@@ -417,8 +438,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 // Split item: one Q tile (tile 0 of the buffer), this issuer takes the key tiles
                 // j = ti, ti + 2, ...; it still waits for the K and V of every tile as they pass, so
-                // that each of its parity waits is at most one phase ahead of its barrier. A tile's
-                // only consumer commits its kv_empty twice (the barrier expects two arrivals).
+                // that each of its parity waits is at most one phase ahead of its barrier.
                 const uint64_t dq = dq_tile0 + qb * ((2 * C::Q_TILE) >> 4);
                 int prev_j = -1;                                  // own tile whose P.V is pending
                 uint32_t prev_st = 0, prev_ph = 0, prev_c = 0;
@@ -435,27 +455,40 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         pv_tail<NSLAB, C::KV_SLAB, D>(tO, tP, dv0 + prev_st * STAGE_STEP,
                                                       base + C::OFF_V + prev_st * C::KV_TILE, acc,
                                                       item.y - prev_j * BN, a_pvdone);
-                    mma_commit(bar_addr(bars.kv_empty[prev_st]));
-                    mma_commit(bar_addr(bars.kv_empty[prev_st]));
+                    mma_commit(bar_addr(bars.v_empty[prev_st]));
                     first_pv = false;
                     return true;
                 };
-                // With three ring slots the next own tile's QK goes out before the pending P.V, as in
-                // the two-tile path; with two, the pending tile's slot must be released first, since
-                // the next own tile's K is loaded into it.
-                constexpr bool qk_first = ST >= 3;
+                // as in the two-tile path, the next own tile's QK goes out before the pending P.V: its
+                // K half of the ring slot is released by QKs only, never by a P.V
+                // the other issuer's tiles: this issuer passes each phase of their K and V as well
+                // and adds its arrival to the slot's release, so the producer never refills a slot
+                // this issuer has not yet seen (its V phase is taken after this issuer's next QK)
+                bool skip_v = false;
+                uint32_t skip_st = 0, skip_ph = 0;
+                auto pass_skipped_v = [&]() -> bool {
+                    if (!skip_v) return true;
+                    if (!(ok = wait(bars.v_full[skip_st], skip_ph))) return false;
+                    mbar_arrive(bar_addr(bars.v_empty[skip_st]));
+                    skip_v = false;
+                    return true;
+                };
                 for (int j = 0; j < n_kv; ++j) {
                     if ((j & 1) != ti) {
                         if (!(ok = wait(bars.k_full[st], ph))) break;
-                        if (!(ok = wait(bars.v_full[st], ph))) break;
+                        mbar_arrive(bar_addr(bars.k_empty[st]));
+                        skip_v = true;
+                        skip_st = st;
+                        skip_ph = ph;
                     } else {
-                        if (!qk_first && prev_j >= 0 && !pv_of_prev()) break;
                         if (!(ok = wait(bars.k_full[st], ph))) break;
                         if (c > 0 && !(ok = wait(b_sfree, (c - 1) & 1))) break;
                         tc_fence_after();
                         qk(dq, dk0 + st * STAGE_STEP);
+                        mma_commit(bar_addr(bars.k_empty[st]));
                         if (j + 2 >= n_kv) mma_commit(bar_addr(bars.q_empty[qb]));   // last own QK
-                        if (qk_first && prev_j >= 0 && !pv_of_prev()) break;
+                        if (!pass_skipped_v()) break;
+                        if (prev_j >= 0 && !pv_of_prev()) break;
                         prev_j = j;
                         prev_st = st;
                         prev_ph = ph;
@@ -467,13 +500,15 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
                 if (!ok) break;
+                // no key tile of this item is this issuer's (a single-tile segment): release the Q
+                // buffer at once (the producer may be waiting for it before it issues the V that
+                // the line below waits for)
+                if (prev_j < 0) mbar_arrive(bar_addr(bars.q_empty[qb]));
+                if (!pass_skipped_v()) break;                  // the item's last tile was the other's
                 if (prev_j >= 0) {
                     if (!pv_of_prev()) break;
-                } else {
-                    // no key tile of this item is this issuer's (a single-tile segment): release the
-                    // Q buffer, and keep o_free's phase count in step with the items
-                    mbar_arrive(bar_addr(bars.q_empty[qb]));
-                    if (item_cnt > 0 && !(ok = wait(b_ofree, (item_cnt - 1) & 1))) break;
+                } else if (item_cnt > 0 && !(ok = wait(b_ofree, (item_cnt - 1) & 1))) {
+                    break;                                     // keep o_free's phase count in step
                 }
                 t += n_kv;
             }
