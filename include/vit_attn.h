@@ -347,7 +347,8 @@ vit_status_t vit_varlen_attn_padded(const void *q, const void *k, const void *v,
  * workspace pair: the scheduler's work list lives instead in a static device
  * array of VIT_NOALLOC_WORKSPACE_BYTES (4 MiB) inside this library, which
  * every GPU that loads the library keeps while its CUDA context lives (until
- * process exit, unless the context is reset). The call itself allocates
+ * process exit, unless the context is reset; with CUDA's lazy module loading
+ * the array is placed when the first call looks it up). The call itself allocates
  * nothing (no cudaMalloc, no cudaFree, no library allocator), and its output
  * is bit-identical to vit_varlen_attn's on the same inputs.
  *   - Limit: sizes whose work list needs more than VIT_NOALLOC_WORKSPACE_BYTES

@@ -198,6 +198,22 @@ def test_release_library_exports_no_test_hook_or_global_setting(L):
     assert "vit_debug_stall_long_kernel" not in open(HEADER).read()
 
 
+def test_test_build_keeps_the_launch_path():
+    # the failure-path hook only exists in the test build; that build must still launch the
+    # tcgen05 kernel (its call site takes the hook's value), which the object's symbols show
+    import shutil
+    import subprocess
+    lib = _build.build_test_hooks()
+    T = ctypes.CDLL(lib)
+    assert hasattr(T, "vit_debug_stall_long_kernel")
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    syms = subprocess.run([nm, "-C", os.path.join(_build.BUILD, "api.cu.testhooks.o")], capture_output=True,
+                          text=True).stdout
+    assert "U vit::launch_attn_long(" in syms and "vit_debug_stall_long_kernel" in syms
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import importlib
     monkeypatch.setattr(vit, "_lib", None)

@@ -64,7 +64,7 @@ constexpr int kDefaultShortMax = 64;
 #ifdef VIT_TEST_HOOKS
 // Test builds only: when set, the long-segment kernel never loads V, so its bounded waits expire.
 std::atomic<int> g_stall_v{0};
-int stall_v() { return stall_v(); }
+int stall_v() { return g_stall_v.load(); }
 #else
 constexpr int stall_v() { return 0; }
 #endif
