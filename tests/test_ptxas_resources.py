@@ -71,10 +71,13 @@ def test_tcgen05_kernel_register_count_matches_its_split(kernels):
     with open(os.path.join(_build.CSRC, "attn_long.cu")) as f:
         src = f.read()
     threads, launch = _constant(src, "kThreads"), _constant(src, "kLaunchRegs")
-    ctrl, softmax = _constant(src, "kCtrlRegs"), _constant(src, "kSoftmaxRegs")
-    # one control warpgroup and the rest softmax warpgroups, 128 threads each: the split may
-    # not draw more than the launch holds (setmaxnreg.inc would wait for registers forever)
-    assert ctrl * 128 + softmax * (threads - 128) <= launch * threads
+    # one control warpgroup and the rest softmax warpgroups, 128 threads each: neither split (the
+    # plain one, and the one of the variant that rotates raw Q) may draw more than the launch
+    # holds (setmaxnreg.inc would wait for registers forever)
+    for ctrl_name, softmax_name in (("kCtrlRegs", "kSoftmaxRegs"), ("kCtrlRegsFQ", "kSoftmaxRegsFQ")):
+        ctrl, softmax = _constant(src, ctrl_name), _constant(src, softmax_name)
+        assert ctrl * 128 + softmax * (threads - 128) <= launch * threads
+        assert ctrl % 8 == 0 and softmax % 8 == 0
     assert launch * threads <= 65536 and launch % 8 == 0
     long_k = [k for k in kernels if "attn_long_kernel" in k["name"]]
     assert long_k

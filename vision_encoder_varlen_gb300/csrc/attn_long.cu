@@ -14,10 +14,14 @@
 // batch too small to occupy the GPU otherwise). Persistent CTAs (one per SM)
 // walk the scheduler's longest-first list. Three warpgroups (384 threads,
 // launched at 168 registers; setmaxnreg lowers the control warpgroup to 88
-// and raises the two softmax warpgroups to 208):
+// and raises the two softmax warpgroups to 208, or 96 and 200 in the variant
+// that rotates raw Q in warp 3):
 //   warp 0      TMA producer: Q tiles per item, K and V tiles into a ring of
-//               STAGES slots; 16-column (32-byte) slabs with 32-byte swizzle,
-//               so any head_dim that is a multiple of 16 maps exactly.
+//               STAGES slots, each tile's V after the next tile's K. Q and K
+//               in 64-column slabs with 128-byte swizzle plus a 16- or
+//               32-column remainder slab (wide boxes stream faster); V in
+//               16-column slabs with 32-byte swizzle (the P.V operand's N is
+//               the head dim, whole swizzle atoms per instruction).
 //   warp 1      TMEM owner; lane 0 issues the MMAs of Q tile 0
 //   warp 2      lane 0 issues the MMAs of Q tile 1
 //                 S_i = Q_i K^T     (SS MMA, M=128, N=BN, K=D)   into TMEM
@@ -61,7 +65,11 @@ constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;              // 65536 / 384, rounded down to a multiple of 8
 constexpr int kCtrlRegs = 88;                 // control warpgroup after setmaxnreg.dec
 constexpr int kSoftmaxRegs = 208;             // softmax warpgroups after setmaxnreg.inc
+// the variant that rotates raw Q in warp 3 gives the control warpgroup more room
+constexpr int kCtrlRegsFQ = 96;
+constexpr int kSoftmaxRegsFQ = 200;
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split exceeds the launch pool");
+static_assert(128 * kCtrlRegsFQ + 256 * kSoftmaxRegsFQ <= kThreads * kLaunchRegs, "register split exceeds the launch pool");
 constexpr int BM = 128;                       // rows per Q tile; two tiles per item
 constexpr long long kWaitBudget = 4000000000ll;   // clock cycles before a wait gives up (~2 s)
 constexpr int kMaxStages = 4;                 // K/V ring slots the barrier arrays hold
@@ -76,16 +84,26 @@ template <int D> struct LongCfg {
     // buffer); the next item's Q pair is prefetched into a second Q buffer where that fits in
     // shared memory (every supported head dim)
     static constexpr int STAGES = D >= 128 ? 2 : 3;
-    static constexpr int QBUF =
-        (4 * (D / 16) * BM * 32 + STAGES * 2 * (D / 16) * BN * 32 + 1024 <= 227 * 1024) ? 2 : 1;
-    static constexpr int NSLAB = D / 16;
-    static constexpr int Q_SLAB = BM * 32;                 // bytes of one 16-column slab of a Q tile
-    static constexpr int KV_SLAB = BN * 32;
-    static constexpr int Q_TILE = NSLAB * Q_SLAB;
-    static constexpr int KV_TILE = NSLAB * KV_SLAB;
+    // Q and K (K-major operands of QK) sit in 64-column slabs with 128-byte swizzle, the columns
+    // past the last multiple of 64 (16 or 32) in one slab with 32- or 64-byte swizzle: a wide TMA box
+    // moves a tile at about 1.6x the rate of 16-column boxes. V (the MN-major operand of P.V, whose
+    // N = head_dim must be whole swizzle atoms in one instruction) keeps 16-column slabs.
+    static constexpr int N128 = D / 64;                     // 64-column slabs
+    static constexpr int REM = D % 64;                      // columns of the remainder slab: 0, 16, 32
+    static constexpr int REM_SW = REM == 32 ? 64 : 32;      // its swizzle width in bytes
+    static constexpr int NK = D / 16;                       // K steps of QK (16 columns each)
+    static constexpr int Q_SLAB128 = BM * 128;
+    static constexpr int K_SLAB128 = BN * 128;
+    static constexpr int Q_TILE = BM * D * 2;
+    static constexpr int K_TILE = BN * D * 2;
+    static constexpr int K_STRIDE = (K_TILE + 1023) / 1024 * 1024;   // ring slots stay 1024-aligned
+    static constexpr int NSLAB = D / 16;                    // 16-column slabs of a V tile
+    static constexpr int KV_SLAB = BN * 32;                 // bytes of one 16-column V slab
+    static constexpr int KV_TILE = NSLAB * KV_SLAB;         // bytes of one V tile
+    static constexpr int QBUF = (4 * Q_TILE + STAGES * (K_STRIDE + KV_TILE) + 1024 <= 227 * 1024) ? 2 : 1;
     static constexpr int OFF_Q = 0;                        // QBUF buffers x two tiles
     static constexpr int OFF_K = OFF_Q + QBUF * 2 * Q_TILE;
-    static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
+    static constexpr int OFF_V = OFF_K + STAGES * K_STRIDE;
     static constexpr int DATA = OFF_V + STAGES * KV_TILE;
     // > half of the SM's shared memory: exactly one CTA (one TMEM owner) per SM
     static constexpr int SMEM = (DATA + 1024 > 118 * 1024) ? DATA + 1024 : 118 * 1024;
@@ -98,7 +116,24 @@ template <int D> struct LongCfg {
     static_assert(SMEM <= 227 * 1024, "shared memory per block (227 KB opt-in limit)");
     static_assert(STAGES >= 2 && STAGES <= kMaxStages, "ring slots the barrier arrays hold");
     static_assert(D % 16 == 0 && BN % 16 == 0 && (BN / 2) % 8 == 0, "tile shapes");
+    static_assert(Q_TILE % 1024 == 0 && K_SLAB128 % 1024 == 0 && OFF_V % 1024 == 0,
+                  "128-byte-swizzle slabs start on 1024-byte boundaries");
+    // byte offset of K step kk (16 columns) inside a Q or K tile of `rows` rows, and whether it
+    // lies in a 128-byte-swizzle slab (else in the remainder slab)
+    __host__ __device__ static constexpr bool wide_step(int kk) { return kk < 4 * N128; }
+    __host__ __device__ static constexpr int step_off(int kk, int rows)
+    {
+        return wide_step(kk) ? (kk / 4) * rows * 128 + (kk % 4) * 32 : N128 * rows * 128 + (kk - 4 * N128) * 32;
+    }
 };
+
+// Shared-memory matrix descriptor of a K-major operand slab: 128-byte swizzle (8-row groups of
+// 1024 B) for the 64-column slabs, the remainder slab's own swizzle otherwise.
+template <int SW> __device__ __forceinline__ uint64_t kmajor_desc(uint32_t addr)
+{
+    static_assert(SW == 128 || SW == 64 || SW == 32, "swizzle width");
+    return smem_desc(addr, 16, 8 * SW, SW == 128 ? 2 : (SW == 64 ? 4 : 6));
+}
 
 struct Bars {
     uint64_t q_full[2], q_empty[2], q_ready[2];
@@ -140,7 +175,8 @@ __device__ __forceinline__ void pv_tail(uint32_t tO, uint32_t tP, uint64_t dv, u
 
 template <int D, bool LSE, bool FQ>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
+                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_kr,
                  const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out, int64_t out_stride,
                  float *__restrict__ lse, int H, float scale_log2, WsHeader *__restrict__ hdr,
                  const Item *__restrict__ items, int32_t *status, int stall_v, const rope::QRope qr)
@@ -224,13 +260,24 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         return x.y >= 0;
     };
 
-    if (warp < 4) regs_dec<kCtrlRegs>();
+    if (warp < 4) regs_dec<FQ ? kCtrlRegsFQ : kCtrlRegs>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_qr);
             tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_kr);
             tma_prefetch_desc(&tm_v);
+            // one Q or K tile: its 64-column slabs (128-byte swizzle), then the remainder slab
+            auto load_qk_tile = [&](unsigned char *dst, const CUtensorMap *wide, const CUtensorMap *rem, int rows,
+                                    int head, int row, uint32_t bar) {
+#pragma unroll
+                for (int s = 0; s < C::N128; ++s)
+                    tma_load_2d(smem_addr(dst + s * rows * 128), wide, head * D + 64 * s, row, bar);
+                if constexpr (C::REM > 0)
+                    tma_load_2d(smem_addr(dst + C::N128 * rows * 128), rem, head * D + 64 * C::N128, row, bar);
+            };
             uint32_t g = 0, q_it = 0;
             // parity + 1 of the last load issued on each barrier (0 = none), for the abort drain;
             // two bits per stage, kept in registers
@@ -241,9 +288,8 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const int nt = split ? 1 : 2;
                 mbar_arrive_expect_tx(bar_addr(bars.q_full[qb]), nt * C::Q_TILE);
                 for (int i = 0; i < nt; ++i)
-                    for (int s = 0; s < NSLAB; ++s)
-                        tma_load_2d(smem_addr(base + C::OFF_Q + (2 * qb + i) * C::Q_TILE + s * C::Q_SLAB), &tm_q,
-                                    head * D + 16 * s, q0 + BM * i, bar_addr(bars.q_full[qb]));
+                    load_qk_tile(base + C::OFF_Q + (2 * qb + i) * C::Q_TILE, &tm_q, &tm_qr, BM, head, q0 + BM * i,
+                                 bar_addr(bars.q_full[qb]));
                 q_pend = (q_pend & ~(3u << (2 * qb))) | (((qn & 1) + 1) << (2 * qb));
             };
             // K and V of a tile go into separate halves of a ring slot: a slot's K half is free once
@@ -309,10 +355,9 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const int st = g % ST;
                     if (g >= (uint32_t)ST && !(ok = wait(bars.k_empty[st], (g / ST - 1) & 1))) break;
                     const int row = seg0 + j * BN;
-                    mbar_arrive_expect_tx(bar_addr(bars.k_full[st]), C::KV_TILE);
-                    for (int s = 0; s < NSLAB; ++s)
-                        tma_load_2d(smem_addr(base + C::OFF_K + st * C::KV_TILE + s * C::KV_SLAB), &tm_k,
-                                    head * D + 16 * s, row, bar_addr(bars.k_full[st]));
+                    mbar_arrive_expect_tx(bar_addr(bars.k_full[st]), C::K_TILE);
+                    load_qk_tile(base + C::OFF_K + st * C::K_STRIDE, &tm_k, &tm_kr, BN, head, row,
+                                 bar_addr(bars.k_full[st]));
                     k_pend = (k_pend & ~(3u << (2 * st))) | ((((g / ST) & 1) + 1) << (2 * st));
                     if (v_row >= 0 && !load_v()) break;
                     v_g = g;
@@ -355,13 +400,18 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int ti = warp - 1;                              // Q tile of this issuer
             constexpr uint32_t ID_QK = idesc_bf16(128, BN, 0, 0);
             constexpr uint32_t ID_PV = idesc_bf16(128, D, 0, 1);
-            constexpr uint32_t STAGE_STEP = C::KV_TILE >> 4;
+            constexpr uint32_t STAGE_STEP = C::KV_TILE >> 4;         // V ring slot, descriptor units
+            constexpr uint32_t K_STEP = C::K_STRIDE >> 4;             // K ring slot
             const uint32_t tS = tmem + (ti ? C::TS1 : C::TS0);
             const uint32_t tO = tmem + (ti ? C::TO1 : C::TO0);
             const uint32_t tP = tmem + (ti ? C::TP1 : C::TP0);
-            const uint64_t dq_own = smem_desc(smem_addr(base + C::OFF_Q + ti * C::Q_TILE), 16, 256, 6);
-            const uint64_t dq_tile0 = smem_desc(smem_addr(base + C::OFF_Q), 16, 256, 6);
-            const uint64_t dk0 = smem_desc(smem_addr(base + C::OFF_K), 16, 256, 6);
+            // descriptor bases (128-byte-swizzle form and remainder form) of this issuer's Q tile, of
+            // tile 0 (split items), and of K ring slot 0; K steps add their offsets in 16-byte units
+            const uint32_t a_q = smem_addr(base + C::OFF_Q), a_k = smem_addr(base + C::OFF_K);
+            const uint64_t dqw_own = kmajor_desc<128>(a_q + ti * C::Q_TILE);
+            const uint64_t dqr_own = kmajor_desc<C::REM_SW>(a_q + ti * C::Q_TILE);
+            const uint64_t dqw_tile0 = kmajor_desc<128>(a_q), dqr_tile0 = kmajor_desc<C::REM_SW>(a_q);
+            const uint64_t dkw0 = kmajor_desc<128>(a_k), dkr0 = kmajor_desc<C::REM_SW>(a_k);
             const uint64_t dv0 = smem_desc(smem_addr(base + C::OFF_V), C::KV_SLAB, 256, 6);
             const uint64_t &b_sfree = bars.s_free[ti], &b_pfull = bars.p_full[ti], &b_ofree = bars.o_free[ti];
             const uint32_t a_sfull = bar_addr(bars.s_full[ti]), a_pvdone = bar_addr(bars.pv_done[ti]);
@@ -370,11 +420,14 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             uint32_t t = 0, c = 0, item_cnt = 0;
             bool ok = true;
 
-            auto qk = [&](uint64_t dq, uint64_t dk) {
+            // S = Q K^T over the K steps: each step's A and B descriptors in the form of its slab
+            auto qk = [&](uint64_t dqw, uint64_t dqr, uint64_t dkw, uint64_t dkr) {
 #pragma unroll
-                for (int kk = 0; kk < NSLAB; ++kk)
-                    mma_ss(tS, dq + (uint64_t)(kk * (C::Q_SLAB >> 4)), dk + (uint64_t)(kk * (C::KV_SLAB >> 4)), ID_QK,
-                           kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < C::NK; ++kk) {
+                    const uint64_t a = (C::wide_step(kk) ? dqw : dqr) + (uint64_t)(C::step_off(kk, BM) >> 4);
+                    const uint64_t b = (C::wide_step(kk) ? dkw : dkr) + (uint64_t)(C::step_off(kk, BN) >> 4);
+                    mma_ss(tS, a, b, ID_QK, kk > 0 ? 1u : 0u);
+                }
                 mma_commit(a_sfull);
             };
             auto pv = [&](uint64_t dv, uint32_t acc) {
@@ -391,12 +444,13 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const uint32_t qb = item_cnt % C::QBUF;         // Q buffer of this item
                 if (!(ok = wait(FQ ? bars.q_ready[qb] : bars.q_full[qb], (item_cnt / C::QBUF) & 1))) break;
                 if (!item_split(item)) {
-                    const uint64_t dq = dq_own + qb * ((2 * C::Q_TILE) >> 4);
+                    const uint64_t qoff = qb * ((2 * C::Q_TILE) >> 4);
+                    const uint64_t dqw = dqw_own + qoff, dqr = dqr_own + qoff;
                     // prologue: S of the item's first key tile
                     if (!(ok = wait(bars.k_full[st], ph))) break;
                     if (c > 0 && !(ok = wait(b_sfree, (c - 1) & 1))) break;
                     tc_fence_after();
-                    qk(dq, dk0 + st * STAGE_STEP);
+                    qk(dqw, dqr, dkw0 + st * K_STEP, dkr0 + st * K_STEP);
                     mma_commit(bar_addr(bars.k_empty[st]));
                     if (n_kv == 1) mma_commit(bar_addr(bars.q_empty[qb]));
                     // one key tile: QK of the next tile, then P.V of this one; the tail variant (the
@@ -410,7 +464,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             if (!(ok = wait(bars.k_full[st1], ph1))) return false;
                             if (!(ok = wait(b_sfree, u & 1))) return false;
                             tc_fence_after();
-                            qk(dq, dk0 + st1 * STAGE_STEP);
+                            qk(dqw, dqr, dkw0 + st1 * K_STEP, dkr0 + st1 * K_STEP);
                             mma_commit(bar_addr(bars.k_empty[st1]));
                             if (j + 2 == n_kv) mma_commit(bar_addr(bars.q_empty[qb]));
                         }
@@ -439,7 +493,8 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // Split item: one Q tile (tile 0 of the buffer), this issuer takes the key tiles
                 // j = ti, ti + 2, ...; it still waits for the K and V of every tile as they pass, so
                 // that each of its parity waits is at most one phase ahead of its barrier.
-                const uint64_t dq = dq_tile0 + qb * ((2 * C::Q_TILE) >> 4);
+                const uint64_t qoff = qb * ((2 * C::Q_TILE) >> 4);
+                const uint64_t dqw = dqw_tile0 + qoff, dqr = dqr_tile0 + qoff;
                 int prev_j = -1;                                  // own tile whose P.V is pending
                 uint32_t prev_st = 0, prev_ph = 0, prev_c = 0;
                 bool first_pv = true;
@@ -484,7 +539,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         if (!(ok = wait(bars.k_full[st], ph))) break;
                         if (c > 0 && !(ok = wait(b_sfree, (c - 1) & 1))) break;
                         tc_fence_after();
-                        qk(dq, dk0 + st * STAGE_STEP);
+                        qk(dqw, dqr, dkw0 + st * K_STEP, dkr0 + st * K_STEP);
                         mma_commit(bar_addr(bars.k_empty[st]));
                         if (j + 2 >= n_kv) mma_commit(bar_addr(bars.q_empty[qb]));   // last own QK
                         if (!pass_skipped_v()) break;
@@ -536,10 +591,16 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const int row = lane + 32 * k;
                     if (q0 + row >= seg_end) continue;
                     const int r = row % BM;
-                    unsigned char *tile = qbuf + (row / BM) * C::Q_TILE + 32 * r;
-                    const int sw = ((r >> 2) & 1) << 4;
-                    rope::transform_row<D>(qr, q0 + row, [&](int c) {
-                        return reinterpret_cast<uint4 *>(tile + (c >> 1) * C::Q_SLAB + (((c & 1) << 4) ^ sw));
+                    unsigned char *tile = qbuf + (row / BM) * C::Q_TILE;
+                    // 16-byte chunk c (columns 8c .. 8c + 7) of row r, through the swizzle the TMA wrote
+                    // (chunk index XOR the row's bits 0-2, 1-2 or 2 for 128-, 64- or 32-byte swizzle)
+                    unsigned char *wide_row = tile + 128 * r;                    // row r of slab 0
+                    unsigned char *rem_row = tile + C::N128 * C::Q_SLAB128 + 2 * C::REM * r;
+                    const int wx = r & 7, rx = C::REM == 32 ? (r >> 1) & 3 : (r >> 2) & 1;
+                    rope::transform_row<D>(qr, q0 + row, [&](int c) -> uint4 * {
+                        if (C::REM == 0 || c < 8 * C::N128)
+                            return reinterpret_cast<uint4 *>(wide_row + (c >> 3) * C::Q_SLAB128 + (((c & 7) ^ wx) << 4));
+                        return reinterpret_cast<uint4 *>(rem_row + (((c - 8 * C::N128) ^ rx) << 4));
                     });
                 }
                 fence_proxy_async_smem();
@@ -555,7 +616,7 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax groups
-        regs_inc<kSoftmaxRegs>();
+        regs_inc<FQ ? kSoftmaxRegsFQ : kSoftmaxRegs>();
         const int grp = (warp - 4) >> 2;                       // 0 or 1: which Q tile
         const int quarter = warp & 3;                          // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;                   // row of the tile = TMEM lane
@@ -780,16 +841,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // [T, H*D] bf16 rows with a token stride, read as 16-column slabs of `rows` rows, 32-byte swizzle.
-bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int D, int64_t stride, int rows)
+// [T, H*D] bf16 rows with a token stride, read as boxes of `cols` columns x `rows` rows with the
+// swizzle that matches the box width (128, 64 or 32 bytes).
+bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int D, int64_t stride, int rows, int cols)
 {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)H * D, (cuuint64_t)(T > 0 ? T : 1)};
     cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
-    cuuint32_t box[2] = {16, (cuuint32_t)rows};
+    cuuint32_t box[2] = {(cuuint32_t)cols, (cuuint32_t)rows};
     cuuint32_t es[2] = {1, 1};
+    const CUtensorMapSwizzle sw = cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -797,9 +863,14 @@ template <int D>
 cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, int stall_v, cudaStream_t stream)
 {
     using C = LongCfg<D>;
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.q, a.T, a.H, D, a.q_stride, BM) || !make_map(&mk, a.k, a.T, a.H, D, a.k_stride, C::BN) ||
-        !make_map(&mv, a.v, a.T, a.H, D, a.v_stride, C::BN))
+    // Q and K: 64-column boxes and a remainder box (unused when head_dim is a multiple of 64);
+    // V: 16-column boxes
+    const int rem = C::REM > 0 ? C::REM : 64;
+    CUtensorMap mq, mqr, mk, mkr, mv;
+    if (!make_map(&mq, a.q, a.T, a.H, D, a.q_stride, BM, 64) || !make_map(&mqr, a.q, a.T, a.H, D, a.q_stride, BM, rem) ||
+        !make_map(&mk, a.k, a.T, a.H, D, a.k_stride, C::BN, 64) ||
+        !make_map(&mkr, a.k, a.T, a.H, D, a.k_stride, C::BN, rem) ||
+        !make_map(&mv, a.v, a.T, a.H, D, a.v_stride, C::BN, 16))
         return cudaErrorInvalidValue;
     // the lse store is compiled in only where it is asked for: the plain kernel keeps its code unchanged
     auto kern = a.lse ? (a.fuse_q ? attn_long_kernel<D, true, true> : attn_long_kernel<D, true, false>)
@@ -819,7 +890,7 @@ cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, int stal
     const unsigned blocks = (unsigned)(max_items < num_sms ? max_items : num_sms);
     if (blocks == 0) return cudaSuccess;
     LaunchScope scope("attn_long", stream);
-    kern<<<blocks, kThreads, C::SMEM, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16 *>(a.out),
+    kern<<<blocks, kThreads, C::SMEM, stream>>>(mq, mqr, mk, mkr, mv, static_cast<__nv_bfloat16 *>(a.out),
                                                                a.out_stride, a.lse, a.H, a.scale_log2,
                                                                const_cast<WsHeader *>(a.hdr),
                                                                a.items, a.status, stall_v, a.qr);
