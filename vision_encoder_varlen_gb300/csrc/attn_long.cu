@@ -826,37 +826,14 @@ attn_long_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// [T, H*D] bf16 rows with a token stride, read as 16-column slabs of `rows` rows, 32-byte swizzle.
 // [T, H*D] bf16 rows with a token stride, read as boxes of `cols` columns x `rows` rows with the
 // swizzle that matches the box width (128, 64 or 32 bytes).
 bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int D, int64_t stride, int rows, int cols)
 {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)H * D, (cuuint64_t)(T > 0 ? T : 1)};
-    cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
-    cuuint32_t box[2] = {(cuuint32_t)cols, (cuuint32_t)rows};
-    cuuint32_t es[2] = {1, 1};
-    const CUtensorMapSwizzle sw = cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                  : cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                               : CU_TENSOR_MAP_SWIZZLE_32B;
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const uint64_t dims[2] = {(uint64_t)H * D, (uint64_t)(T > 0 ? T : 1)};
+    const uint64_t strides[1] = {(uint64_t)stride * 2};
+    const uint32_t box[2] = {(uint32_t)cols, (uint32_t)rows};
+    return encode_tiled_map(m, ptr, 2, dims, strides, box, cols * 2);
 }
 
 template <int D>
@@ -898,6 +875,36 @@ cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, int stal
 }
 
 }  // namespace
+
+bool encode_tiled_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims, const uint64_t *strides,
+                      const uint32_t *box, int swizzle_bytes)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                    cudaSuccess &&
+                q == cudaDriverEntryPointSuccess)
+                   ? reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p)
+                   : nullptr;
+    }();
+    if (!fn || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                  : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(ptr), d, st, bx, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int attn_long_bm() { return 2 * BM; }
 

@@ -1,6 +1,7 @@
 // Internal declarations shared by the CUDA translation units of libvitattn.
 #pragma once
 
+#include <cuda.h>           // CUtensorMap (type only; the library never links libcuda)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -137,6 +138,12 @@ vit_status_t check_varlen_attn_args(const void *q, const void *k, const void *v,
                                     const int32_t *seq_len, int B, int max_seqlen, float scale, const void *out,
                                     int64_t out_stride, const float *lse, const vit_attn_options_t *opts,
                                     bool *nothing);
+
+// A tiled TMA descriptor of a bf16 tensor (cuTensorMapEncodeTiled, reached through the runtime's
+// driver entry point): `rank` dims innermost first, rank - 1 byte strides of the outer dims, the
+// box, and the swizzle span in bytes (32, 64, 128; anything else: none). False when it fails.
+bool encode_tiled_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims, const uint64_t *strides,
+                      const uint32_t *box, int swizzle_bytes);
 
 // VIT_OK when the current device is one this library was built for.
 vit_status_t check_device();
