@@ -268,9 +268,10 @@ def load_traffic(kernel: str, workload: str):
 
 def kernel_algorithmic_flops(w: wl.Workload, kernel: str, short_max: int) -> float:
     """Useful flops a kernel processes per step: 4 L^2 H D over the segments it owns
-    (attn_long: segments longer than short_max tokens; attn_short: the rest)."""
+    (attn_long: segments longer than min(short_max, 64) tokens; attn_tiny: the rest)."""
+    tiny_max = min(short_max, 64)
     L = w.lengths.astype(np.float64)
-    L = L[L > short_max] if kernel == "attn_long" else L[L <= short_max]
+    L = L[L > tiny_max] if kernel == "attn_long" else L[L <= tiny_max]
     return float(4.0 * np.sum(L * L) * w.heads * w.head_dim)
 
 
@@ -376,8 +377,6 @@ def roofline_entry(vit, w: wl.Workload, kt: dict, short_max: int, peaks: dict, p
     L = w.lengths
     if dom == "attn_tiny":           # q, k, v read and out written once per token it owns
         alg = 8.0 * float(L[L <= tiny_max].sum()) * H * D
-    elif dom == "attn_short":
-        alg = 8.0 * float(L[(L > tiny_max) & (L <= short_max)].sum()) * H * D
     elif dom == "qk_norm_rope":      # q and k (k alone with --fused-q) read and written once
         alg = (4.0 if fused_q else 8.0) * T * H * D
     else:
@@ -536,14 +535,15 @@ def run_ours(args, rank, world, local):
 
 
 def run_split_sweep(args):
-    """Attention time with every segment on the warp-MMA kernel vs every segment on the tcgen05
-    kernel, for bands of random segment lengths (one JSON line per band and head_dim)."""
+    """Attention time with every segment on the tiny-segment (warp-MMA) kernel vs every segment on
+    the tcgen05 kernel, for bands of random segment lengths up to the tiny kernel's 64 tokens (one
+    JSON line per band and head_dim)."""
     import vision_encoder_varlen_gb300 as vit
     from vision_encoder_varlen_gb300 import _build
     _build.build()
     rng = np.random.default_rng(0)
     for D in (80, 128):
-        for lo, hi in ((4, 16), (16, 32), (32, 64), (64, 128), (128, 256), (256, 512)):
+        for lo, hi in ((4, 16), (16, 32), (32, 64)):
             lengths = rng.integers(lo, hi + 1, size=8192 if hi <= 32 else (4096 if hi <= 128 else 2048))
             w = wl.from_lengths(lengths, 16, D, max_seqlen_meta=4096)
             g = torch.Generator(device="cuda").manual_seed(1)
@@ -553,7 +553,7 @@ def run_split_sweep(args):
             ws = torch.empty(vit.workspace_size(T, 16, w.num_segments, D), dtype=torch.uint8, device="cuda")
             out = torch.empty_like(q)
             res = {}
-            for name, sm in (("warp_mma_kernels_ms", 1 << 30), ("tcgen05_kernel_ms", 0)):
+            for name, sm in (("tiny_kernel_ms", 64), ("tcgen05_kernel_ms", 0)):
                 for _ in range(args.warmup):
                     vit.varlen_attn(q, k, v, cu, 4096, out=out, workspace=ws, short_max=sm)
                 torch.cuda.synchronize()
@@ -611,7 +611,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5, 6, 7],
                     help="workload 1..5 (default 5); 6 = a single 128x128 image for profiler captures; "
-                         "7 = 4096 small images for the short-segment kernel")
+                         "7 = 4096 small images for the tiny-segment kernel")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -621,7 +621,7 @@ def main():
     ap.add_argument("--sweep-split", action="store_true",
                     help="time both attention kernels over bands of segment lengths and exit")
     ap.add_argument("--short-max", type=int, default=None,
-                    help="segments longer than this run on the tcgen05 kernel (library default 64)")
+                    help="segments longer than min(this, 64) run on the tcgen05 kernel (library default 64)")
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--lse", action="store_true", help="also write the per-row log-sum-exp [T, H] each step")
     ap.add_argument("--fused-q", action="store_true",

@@ -378,15 +378,14 @@ vit_status_t vit_varlen_attn_noalloc(const void *q, const void *k, const void *v
  * how the work is spread over the kernels: results agree within the output
  * tolerance for every setting, and the workspace size does not depend on them.
  *
- *   short_segment_max   kernel split: segments longer than this many tokens run
- *                       on the tcgen05/TMEM long-segment kernel, the others on
- *                       warp-MMA kernels (segments of at most
- *                       min(short_segment_max, 64) tokens on the tiny-segment
- *                       kernel, one item per segment and head; longer ones on
- *                       the short-segment kernel, 128 query rows per item).
- *                       0 sends every segment to the long kernel, INT_MAX every
- *                       segment to the warp-MMA kernels. -1 = library default
- *                       (64, the measured crossover on GB300). Below -1:
+ *   short_segment_max   kernel split: segments of at most
+ *                       min(short_segment_max, 64) tokens run on the
+ *                       tiny-segment (warp-MMA) kernel, one item per segment
+ *                       and a few heads; longer ones on the tcgen05/TMEM
+ *                       long-segment kernel. 0 sends every segment to the long
+ *                       kernel; values above 64 act as 64 (the tiny kernel's
+ *                       bound; above it the long kernel is the faster one on
+ *                       GB300). -1 = library default (64). Below -1:
  *                       VIT_ERR_BAD_ARGUMENT.
  */
 typedef struct vit_attn_options {

@@ -22,7 +22,7 @@ def _built():
 
 # "default" passes no option (the plain entry points, the library's own split); the others pass
 # their split with every call
-SPLITS = {"default": None, "all_long": 0, "all_short": 2 ** 31 - 1}
+SPLITS = {"default": None, "all_long": 0, "split_32": 32}
 
 
 @pytest.fixture(params=list(SPLITS))
@@ -254,21 +254,28 @@ def test_long_kernel_bounded_wait_reports_timeout_and_context_survives():
 def test_threads_with_different_splits_get_their_own_results():
     """The kernel split is a per-call option: two host threads that keep issuing the same
     attention with different splits, on their own streams, each get exactly the bits their own
-    split gives when run alone (the two splits round differently, so a leaked setting shows)."""
+    split gives when run alone. The short segments run on the tiny kernel under one split and on
+    the tcgen05 kernel under the other; their fp32 log-sum-exp rows differ between the two
+    kernels (other summation orders), so a leaked setting shows."""
     import threading
-    w, t, cu, (q, k, v) = _inputs([700, 40, 300, 129], 4, 80, seed=8)
-    splits = (0, 2 ** 31 - 1)
-    alone = {sm: vit.varlen_attn(q, k, v, cu, w.max_seqlen, short_max=sm) for sm in splits}
+    w, t, cu, (q, k, v) = _inputs([700, 40, 64, 300, 17, 129, 50], 8, 80, seed=8)
+    splits = (0, 64)
+
+    def call(sm):
+        out, lse = vit.varlen_attn(q, k, v, cu, w.max_seqlen, short_max=sm, return_lse=True)
+        return out, lse
+
+    alone = {sm: call(sm) for sm in splits}
     torch.cuda.synchronize()
-    assert not torch.equal(alone[0], alone[splits[1]])
+    assert not torch.equal(alone[0][1], alone[64][1])
     bad = []
 
     def worker(sm):
         s = torch.cuda.Stream()
         with torch.cuda.stream(s):
-            outs = [vit.varlen_attn(q, k, v, cu, w.max_seqlen, short_max=sm) for _ in range(30)]
+            outs = [call(sm) for _ in range(30)]
         s.synchronize()
-        bad.extend(sm for o in outs if not torch.equal(o, alone[sm]))
+        bad.extend(sm for o, l in outs if not (torch.equal(o, alone[sm][0]) and torch.equal(l, alone[sm][1])))
 
     th = [threading.Thread(target=worker, args=(sm,)) for sm in splits]
     for x in th:

@@ -29,7 +29,7 @@ PATH_MAX_ABS, PATH_MEAN_ABS = 2e-2, 2e-3
 
 # "default" passes no option (the plain entry points, the library's own split); the others pass
 # their split with every call
-SPLITS = {"default": None, "all_long": 0, "all_short": 2 ** 31 - 1}
+SPLITS = {"default": None, "all_long": 0, "split_32": 32}
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 # "default" passes no option (the plain entry points, the library's own split); the others pass
 # their split with every call
-SPLITS = {"default": None, "all_long": 0, "all_short": 2 ** 31 - 1}
+SPLITS = {"default": None, "all_long": 0, "split_32": 32}
 NAN_BF16 = 0x7FC0
 SENTINEL = 0x1234
 

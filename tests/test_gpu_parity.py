@@ -127,7 +127,7 @@ LENGTH_CASES = [
 
 # "default" passes no option (the plain entry points, the library's own split); the others pass
 # their split with every call
-SPLITS = {"default": None, "all_long": 0, "all_short": 2 ** 31 - 1}
+SPLITS = {"default": None, "all_long": 0, "split_32": 32}
 
 
 @pytest.fixture(params=list(SPLITS))

@@ -1,16 +1,15 @@
 """The device scheduler's work list, bit for bit against a host recomputation.
 
-After a call, the workspace holds a 64-byte header (int32: long items, short
-items, rows per long item, rows per short item, error, tiny items, whether
-every long item is split) and the items (int4: segment start, segment length,
-first query row, head | split flag). The host recomputes the same list from the
-segment lengths and the SM count alone: segments longer than the split go to
-the tcgen05 kernel in 256-row blocks, longest first (ties by index), a last
-block of at most 128 rows flagged as split; when that would give at most
-SMs / 2 long items, every long segment goes in 128-row blocks instead, all
-flagged. The rest follow in index order, those of at most min(split, 64)
-tokens last, one item per head; heads outer, query blocks inner within a
-segment."""
+After a call, the workspace holds a 64-byte header (int32: long items, 0, rows
+per long item, the tiny bound, error, tiny items, whether every long item is
+split) and the items (int4: segment start, segment length, first query row,
+head | split flag). The host recomputes the same list from the segment lengths
+and the SM count alone: segments longer than min(split, 64) go to the tcgen05
+kernel in 256-row blocks, longest first (ties by index), a last block of at
+most 128 rows flagged as split; when that would give at most SMs / 2 long
+items, every long segment goes in 128-row blocks instead, all flagged. The
+rest (tiny segments) follow in index order, one item per head; heads outer,
+query blocks inner within a segment."""
 import numpy as np
 import pytest
 import torch
@@ -20,7 +19,7 @@ from vision_encoder_varlen_gb300 import _build
 
 pytestmark = pytest.mark.gpu
 
-BM_LONG, BM_SHORT, TINY = 256, 128, 64
+BM_LONG, TINY = 256, 64
 SPLIT = 1 << 30
 
 
@@ -34,14 +33,13 @@ def _built():
 def expected(lengths, starts, H, short_max, num_sms):
     tiny_max = min(short_max, TINY)
     idx = range(len(lengths))
-    long_s = sorted((i for i in idx if lengths[i] > short_max), key=lambda i: (-lengths[i], i))
-    short_s = [i for i in idx if tiny_max < lengths[i] <= short_max]
+    long_s = sorted((i for i in idx if lengths[i] > tiny_max), key=lambda i: (-lengths[i], i))
     tiny_s = [i for i in idx if lengths[i] <= tiny_max]
     full_items = sum(H * -(-int(lengths[i]) // BM_LONG) for i in long_s)
     all_split = 2 * full_items <= num_sms
     bm_long = BM_LONG // 2 if all_split else BM_LONG
     items, counts = [], []
-    for group, bm in ((long_s, bm_long), (short_s, BM_SHORT), (tiny_s, BM_SHORT)):
+    for group, bm in ((long_s, bm_long), (tiny_s, TINY)):
         n0 = len(items)
         for seg in group:
             L, a = int(lengths[seg]), int(starts[seg])
@@ -102,17 +100,17 @@ CASES = [
 
 
 @pytest.mark.parametrize("padded", [False, True])
-@pytest.mark.parametrize("short_max", [64, 0, 2 ** 31 - 1, 100])
+@pytest.mark.parametrize("short_max", [64, 0, 2 ** 31 - 1, 100, 32])
 @pytest.mark.parametrize("lengths,H", CASES)
 def test_work_list_matches_host_recomputation(lengths, H, short_max, padded):
     hdr, items, starts = run(lengths, H, 80, short_max, padded)
     counts, ref, bm_long, all_split = expected(np.asarray(lengths), starts, H, short_max, _num_sms())
     n = sum(counts)
     assert hdr[4] == 0                                     # no error
-    assert (hdr[0], hdr[1], hdr[5]) == tuple(counts)
+    assert (hdr[0], hdr[1], hdr[5]) == (counts[0], 0, counts[1])
     if counts[0]:
         assert hdr[2] == bm_long and hdr[6] == int(all_split)
-    assert hdr[3] == BM_SHORT
+    assert hdr[3] == min(short_max, TINY)
     assert np.array_equal(items[:n], ref)
 
 
@@ -132,5 +130,5 @@ def test_work_list_many_segments():
     lengths[rng.choice(3000, 20, replace=False)] = rng.integers(1000, 5000, size=20)
     hdr, items, starts = run(lengths, 2, 64, 64)
     counts, ref, _, _ = expected(lengths, starts, 2, 64, _num_sms())
-    assert (hdr[0], hdr[1], hdr[5]) == tuple(counts)
+    assert (hdr[0], hdr[1], hdr[5]) == (counts[0], 0, counts[1])
     assert np.array_equal(items[:sum(counts)], ref)

@@ -50,7 +50,7 @@ def kernels(tmp_path_factory):
 
 def test_every_kernel_is_reported(kernels):
     names = " ".join(k["name"] for k in kernels)
-    for kern in ("attn_long_kernel", "attn_short_kernel", "attn_tiny_kernel", "qk_norm_rope_kernel",
+    for kern in ("attn_long_kernel", "attn_tiny_kernel", "qk_norm_rope_kernel",
                  "qk_norm_rope_staged_kernel", "rope_freqs_kernel", "rope_table_kernel", "schedule_kernel"):
         assert kern in names, kern
 

@@ -98,7 +98,8 @@ _tls = threading.local()
 @contextlib.contextmanager
 def kernel_split(short_max: int | None):
     """Within the block, attention calls made by this thread pass ``short_max`` as their kernel
-    split (segments longer than it run on the tcgen05 kernel); None restores the library default.
+    split (segments longer than min(short_max, 64) run on the tcgen05 kernel, the others on the
+    tiny-segment kernel); None restores the library default.
     Per thread, and passed with every call: the library itself keeps no setting between calls."""
     prev = getattr(_tls, "short_max", None)
     _tls.short_max = None if short_max is None else int(short_max)

@@ -13,7 +13,6 @@
 
 namespace vit {
 size_t schedule_smem_bytes(int B);
-int attn_short_bm();
 int attn_long_bm();
 int attn_tiny_max();
 }  // namespace vit
@@ -56,9 +55,9 @@ vit_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? VIT_OK : VIT_E
 constexpr int64_t kMaxTokens = (int64_t)1 << 31;
 
 // Segments longer than this run on the tcgen05 long-segment kernel, the others on the
-// warp-MMA kernels, unless a call's options say otherwise. Measured on GB300: up to 64 tokens
-// the tiny-segment kernel is 2-4x faster than the tcgen05 kernel, from 64 tokens up the
-// tcgen05 kernel wins.
+// tiny-segment kernel, unless a call's options ask for a lower split (the tiny kernel takes at
+// most 64 tokens). Measured on GB300: up to 64 tokens the tiny-segment kernel is 2-4x faster
+// than the tcgen05 kernel.
 constexpr int kDefaultShortMax = 64;
 
 #ifdef VIT_TEST_HOOKS
@@ -193,8 +192,8 @@ vit_status_t vit_rope_table(const float *inv_freq, int head_dim, int max_pos, fl
 size_t vit_varlen_attn_workspace_size(int64_t T, int H, int B, int D)
 {
     if (T < 0 || T >= kMaxTokens || H < 1 || B < 0 || B > VIT_MAX_SEGMENTS || !head_dim_ok(D)) return 0;
-    // every work item covers at least 64 query rows (128 for short segments, 256 for long
-    // ones), so this bound holds for any kernel split; item indices are int32 on the device
+    // a tiny segment is one item per head and a long one at least 128 query rows per item, so
+    // this bound holds for any kernel split; item indices are int32 on the device
     const int64_t items = max_items(T, H, B, 64);
     if (items >= ((int64_t)1 << 31)) return 0;
     return sizeof(WsHeader) + sizeof(Item) * (size_t)items;
@@ -289,13 +288,12 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
     WsHeader *hdr = static_cast<WsHeader *>(workspace);
     Item *items = reinterpret_cast<Item *>(hdr + 1);
     SchedParams sp;
-    sp.short_max = (opts && opts->short_segment_max >= 0) ? opts->short_segment_max : kDefaultShortMax;
-    sp.tiny_max = sp.short_max < attn_tiny_max() ? sp.short_max : attn_tiny_max();
+    const int split = (opts && opts->short_segment_max >= 0) ? opts->short_segment_max : kDefaultShortMax;
+    sp.tiny_max = split < attn_tiny_max() ? split : attn_tiny_max();
     sp.bm_long = attn_long_bm();
-    sp.bm_short = attn_short_bm();
     sp.num_sms = sms;
-    // the scheduler divides by these with shifts
-    if ((sp.bm_long & (sp.bm_long - 1)) || (sp.bm_short & (sp.bm_short - 1))) return VIT_ERR_BAD_ARGUMENT;
+    // the scheduler divides by this with shifts
+    if (sp.bm_long & (sp.bm_long - 1)) return VIT_ERR_BAD_ARGUMENT;
     cudaError_t e = launch_schedule(padded ? nullptr : cu_seqlens, seq_start, seq_len, B, T, H, max_seqlen, sp, hdr,
                                     items, status_dev, s);
     if (e != cudaSuccess) return VIT_ERR_CUDA;
@@ -330,17 +328,13 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
     }
     // a segment can only be long when the bound allows it
     const int64_t longest = (cu_seqlens || padded) ? (int64_t)max_seqlen : T / B;
-    if (longest > sp.short_max) {
+    if (longest > sp.tiny_max) {
         // split items cover bm_long / 2 rows, so that many more items may exist
         e = launch_attn_long(a, max_items(T, H, B, sp.bm_long / 2), sms, stall_v(), s);
         if (e != cudaSuccess) return VIT_ERR_CUDA;
     }
-    // segments in (tiny_max, short_max] on the short-segment kernel, the rest of the short ones
-    // on the tiny-segment kernel; a kernel is launched only when its class can be non-empty
-    if (sp.short_max > sp.tiny_max) {
-        e = launch_attn_short(a, max_items(T, H, B, sp.bm_short), sms, s);
-        if (e != cudaSuccess) return VIT_ERR_CUDA;
-    }
+    // segments of at most tiny_max tokens on the tiny-segment kernel (launched only when that
+    // class can be non-empty)
     if (sp.tiny_max > 0) e = launch_attn_tiny(a, (int64_t)H * B, sms, s);
     return from_cuda(e);
 }

@@ -1,6 +1,6 @@
 // Long-segment varlen attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// Same result as the short-segment kernel: for each (segment, head) the plain
+// Same result as the tiny-segment kernel: for each (segment, head) the plain
 // softmax(scale * q k^T) v over that segment's keys only (vLLM Dots
 // vision_attention page, VisionAttentionV2.forward / VisionAttention.forward
 // with its block-diagonal mask), softmax in fp32, P rounded to bf16 for the

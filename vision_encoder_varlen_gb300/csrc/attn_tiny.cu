@@ -136,7 +136,7 @@ attn_tiny_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // a tiny segment has one work item per head, in head order: HG of them make one item here
-    const int n_items = hdr->n_tiny / HG, first = hdr->n_long + hdr->n_short;
+    const int n_items = hdr->n_tiny / HG, first = hdr->n_long;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(bar_addr(&sh.full[i]), 1);

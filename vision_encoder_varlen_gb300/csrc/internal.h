@@ -29,11 +29,11 @@ __host__ __device__ inline bool item_split(const Item &it) { return (it.w & kIte
 // Header at the start of the attention workspace, written by the scheduler.
 struct WsHeader {
     int32_t n_long;      // items [0, n_long) go to the long-segment kernel
-    int32_t n_short;     // items [n_long, n_long + n_short) go to the short-segment kernel
+    int32_t reserved;    // 0
     int32_t bm_long;     // query rows per long item
-    int32_t bm_short;    // query rows per short (and tiny) item
+    int32_t tiny_max;    // segments of at most this many tokens are tiny (one item per head)
     int32_t error;       // device-detected error of the last scheduling pass (0 = none)
-    int32_t n_tiny;      // items [n_long + n_short, + n_tiny) go to the tiny-segment kernel
+    int32_t n_tiny;      // items [n_long, n_long + n_tiny) go to the tiny-segment kernel
     int32_t long_all_split;   // 1 when every long item is a split item of bm_long / 2 rows
     int32_t next_long;   // long items handed out so far beyond each CTA's first (zeroed by the scheduler)
     int32_t pad[8];
@@ -42,10 +42,9 @@ static_assert(sizeof(WsHeader) == 64, "header is 64 bytes");
 
 // Scheduling parameters chosen by the host.
 struct SchedParams {
-    int short_max;   // segments with length <= short_max use a warp-MMA kernel, longer ones the tcgen05 one
-    int tiny_max;    // of those, segments with length <= tiny_max use the tiny-segment kernel
+    int tiny_max;    // segments with length <= tiny_max use the tiny-segment kernel (one item per
+                     // head), longer ones the tcgen05 kernel
     int bm_long;     // q rows per long item
-    int bm_short;    // q rows per short item (a tiny segment is always one item per head)
     int num_sms;     // SMs of the device: with at most num_sms / 2 long items of bm_long rows, every
                      // long block is cut to bm_long / 2 rows and split over its key tiles instead
 };
@@ -122,8 +121,6 @@ struct AttnArgs {
     bool fuse_q;                // q holds raw values: normalise and rotate each Q tile after it is loaded
     rope::QRope qr;             // how (when fuse_q)
 };
-
-cudaError_t launch_attn_short(const AttnArgs &a, int64_t max_items_short, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_attn_tiny(const AttnArgs &a, int64_t max_items_tiny, int num_sms, cudaStream_t stream);
 

@@ -12,18 +12,17 @@
 //      between them are padding that nothing reads or writes;
 //   2. orders the segments: those for the long-segment kernel longest first
 //      (LPT, a bitonic sort of (length desc, index asc) keys, so the order is
-//      deterministic and the persistent CTAs end together), then the short
-//      and the tiny ones in index order (a stable partition by block scans:
-//      their items are small, so sorting them buys no balance and cost most of
-//      the scheduler's time for thousands of small images);
+//      deterministic and the persistent CTAs end together), then the tiny
+//      ones in index order (a stable partition by block scans: their items
+//      are small, so sorting them buys no balance and cost most of the
+//      scheduler's time for thousands of small images);
 //   3. expands every segment into (segment, head, q-block) work items: long
 //      segments into blocks of bm_long query rows for the long-segment kernel
 //      (a last block of at most bm_long / 2 rows, and every block of a batch
 //      too small to give each SM two blocks' worth of items, as a split item
 //      of bm_long / 2 rows whose two halves take alternate key tiles),
-//      short ones into blocks of bm_short rows for the short-segment kernel,
-//      tiny ones (at most tiny_max tokens) into one item per head for the
-//      tiny-segment kernel. Longest first, the three classes come out as three
+//      tiny ones (at most tiny_max tokens) into one item per head, in head
+//      order, for the tiny-segment kernel. The two classes come out as two
 //      contiguous runs of the item list.
 //      Items never straddle two segments; the q-block is the fastest index,
 //      so concurrently running CTAs share one head's K/V in L2.
@@ -112,7 +111,7 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
     if (s_err) {
         if (tid == 0) {
             hdr->n_long = 0;
-            hdr->n_short = 0;
+            hdr->reserved = 0;
             hdr->n_tiny = 0;
             hdr->long_all_split = 0;
             hdr->next_long = 0;
@@ -122,18 +121,17 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
         return;
     }
 
-    // ---- 2. order: long class longest first, then short, then tiny (index order within each)
+    // ---- 2. order: long class longest first, then tiny (index order)
     const int per = (B + kThreads - 1) / kThreads;
     const int lo = min(tid * per, B), hi = min(lo + per, B);
-    auto seg_class = [&](int len) { return len > sp.short_max ? 0 : (len <= sp.tiny_max ? 2 : 1); };
-    int64_t cnt[3] = {0, 0, 0};
+    auto seg_class = [&](int len) { return len > sp.tiny_max ? 0 : 1; };
+    int64_t cnt[2] = {0, 0};
     for (int i = lo; i < hi; ++i) ++cnt[seg_class(s_len[i])];
-    int64_t tot[3];
-    int64_t pos[3];
-    for (int c = 0; c < 3; ++c) pos[c] = block_exclusive_scan(cnt[c], s_warp, &tot[c]);
+    int64_t tot[2];
+    int64_t pos[2];
+    for (int c = 0; c < 2; ++c) pos[c] = block_exclusive_scan(cnt[c], s_warp, &tot[c]);
     const int n_lseg = (int)tot[0];
     pos[1] += tot[0];
-    pos[2] += tot[0] + tot[1];
     for (int i = lo; i < hi; ++i) {
         const int c = seg_class(s_len[i]);
         if (c == 0)      // ascending keys = descending length, then ascending index
@@ -170,33 +168,28 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
     // Long blocks are bm_long rows (two Q tiles) unless the whole batch would give at most
     // num_sms / 2 of them: then every long block is cut to bm_long / 2 rows, twice as many items,
     // each split over its key tiles, so twice as many SMs work on the batch.
-    const int lg_full = __ffs(sp.bm_long) - 1, lg_short = __ffs(sp.bm_short) - 1;
+    const int lg_full = __ffs(sp.bm_long) - 1;
     int64_t local_full = 0, total_full;
     for (int p = lo; p < hi; ++p) {
         const int len = s_len[s_order[p]];
-        if (len > sp.short_max) local_full += (int64_t)H * ((len + (1 << lg_full) - 1) >> lg_full);
+        if (len > sp.tiny_max) local_full += (int64_t)H * ((len + (1 << lg_full) - 1) >> lg_full);
     }
     block_exclusive_scan(local_full, s_warp, &total_full);
     const bool all_split = 2 * total_full <= (int64_t)sp.num_sms;
     const int lg_long = all_split ? lg_full - 1 : lg_full;
-    auto n_blocks = [&](int len) {
-        const int lg = len > sp.short_max ? lg_long : lg_short;
-        return (len + (1 << lg) - 1) >> lg;
+    auto n_blocks = [&](int len) {                      // a tiny segment is one block
+        return len > sp.tiny_max ? (len + (1 << lg_long) - 1) >> lg_long : (len > 0 ? 1 : 0);
     };
-    int64_t local = 0, local_long = 0, local_tiny = 0;
+    int64_t local = 0, local_long = 0;
     for (int p = lo; p < hi; ++p) {
-        const int seg = s_order[p];
-        const int len = s_len[seg];
-        const bool is_long = len > sp.short_max;
+        const int len = s_len[s_order[p]];
         const int64_t n = (int64_t)H * n_blocks(len);
         local += n;
-        if (is_long) local_long += n;
-        else if (len <= sp.tiny_max) local_tiny += n;
+        if (len > sp.tiny_max) local_long += n;
     }
-    int64_t total, total_long, total_tiny;
+    int64_t total, total_long;
     int64_t run = block_exclusive_scan(local, s_warp, &total);
     block_exclusive_scan(local_long, s_warp, &total_long);
-    block_exclusive_scan(local_tiny, s_warp, &total_tiny);
     for (int p = lo; p < hi; ++p) {
         s_off[p] = (int32_t)run;
         run += (int64_t)H * n_blocks(s_len[s_order[p]]);
@@ -208,9 +201,9 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
         const int seg = s_order[p];
         const int len = s_len[seg];
         if (len == 0) continue;
-        const bool is_long = len > sp.short_max;
-        const int bm = is_long ? (1 << lg_long) : sp.bm_short;
-        const int nq = n_blocks(len);
+        const bool is_long = len > sp.tiny_max;
+        const int bm = 1 << lg_long;
+        const int nq = n_blocks(len);             // 1 for a tiny segment
         const int start = s_start[seg];
         // a long item is split when every long item is, or when it is the segment's last block
         // and holds at most bm_long / 2 rows (its second Q tile would be empty)
@@ -229,10 +222,10 @@ schedule_kernel(const int32_t *__restrict__ cu_seqlens, const int32_t *__restric
     }
     if (tid == 0) {
         hdr->n_long = (int32_t)total_long;
-        hdr->n_short = (int32_t)(total - total_long - total_tiny);
-        hdr->n_tiny = (int32_t)total_tiny;
+        hdr->reserved = 0;
+        hdr->n_tiny = (int32_t)(total - total_long);
         hdr->bm_long = 1 << lg_long;
-        hdr->bm_short = sp.bm_short;
+        hdr->tiny_max = sp.tiny_max;
         hdr->error = 0;
         hdr->long_all_split = all_split ? 1 : 0;
         hdr->next_long = 0;

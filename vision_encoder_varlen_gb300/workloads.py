@@ -136,7 +136,7 @@ def make_config(idx: int) -> Workload:
         return Workload("profile_128x128_h16_d80_qknorm", ((128, 128),), 16, 80, True, seed=seed)
     if idx == 7:
         # not one of the five study shapes: 4096 small images (16..64 tokens) that all run on the
-        # short-segment kernel, for its HBM-bandwidth measurement (~1.5 GB of q/k/v/out)
+        # tiny-segment kernel, for its HBM-bandwidth measurement (~1.5 GB of q/k/v/out)
         return Workload("short_4096img_4..8_h16_d80_qknorm", _uniform_grids(rng, 4096, 4, 8, 4, 8), 16, 80, True,
                         seed=seed)
     raise ValueError(f"no workload {idx}")
