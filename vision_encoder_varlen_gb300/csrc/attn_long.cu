@@ -12,7 +12,10 @@
 // halves of the CTA, which merge their partial results at the end (the
 // segment's last block when it has at most 128 rows, and every block of a
 // batch too small to occupy the GPU otherwise). Persistent CTAs (one per SM)
-// walk the scheduler's longest-first list. Three warpgroups (384 threads,
+// take the scheduler's longest-first list in order: each CTA its own index
+// first, then the next unclaimed item from a device counter, which the
+// producer passes to the other roles through a small shared-memory item ring
+// (CTAs that draw short items take more of them). Three warpgroups (384 threads,
 // launched at 168 registers; setmaxnreg lowers the control warpgroup to 88
 // and raises the two softmax warpgroups to 208, or 96 and 200 in the variant
 // that rotates raw Q in warp 3):
