@@ -83,10 +83,10 @@ template <int D> struct LongCfg {
     // keys per tile: the largest multiple of 16 (at most 128) with S0, S1 (BN columns each),
     // O0, O1 (D each) and separate P0, P1 (BN/2 each) inside the 512 TMEM columns
     static constexpr int BN = ((512 - 2 * D) / 3 / 16 * 16 > 128) ? 128 : (512 - 2 * D) / 3 / 16 * 16;
-    // K/V ring of 3 slots (2 at head_dim 128, where three would leave no room for a second Q
-    // buffer); the next item's Q pair is prefetched into a second Q buffer where that fits in
-    // shared memory (every supported head dim)
-    static constexpr int STAGES = D >= 128 ? 2 : 3;
+    // K/V ring of 3 slots; the next item's Q pair is prefetched into a second Q buffer where that
+    // fits in shared memory (every head dim but 128: there a third K/V slot measured 1.8 % faster
+    // than a second Q buffer, since a K tile lands thousands of cycles after its copy is issued)
+    static constexpr int STAGES = 3;
     // Q and K (K-major operands of QK) sit in 64-column slabs with 128-byte swizzle, the columns
     // past the last multiple of 64 (16 or 32) in one slab with 32- or 64-byte swizzle: a wide TMA box
     // moves a tile at about 1.6x the rate of 16-column boxes. V (the MN-major operand of P.V, whose
