@@ -3,7 +3,9 @@
 The kernel's roles talk only through mbarriers: the TMA producer (Q per item, each
 tile's K, then the previous tile's V), the item ring it feeds, two MMA issuers
 (two-tile items, and split items whose key tiles alternate between them), eight
-softmax warps (two groups; split items end with a two-phase merge) and warp 3. This
+softmax warps (two groups; split items end with a two-phase merge; at head_dim 128 a
+two-tile item's output is written after the group has stored the first P of its next
+item, at the other head dims at once) and warp 3. This
 module replays exactly those waits and arrivals as Python generators under a random
 scheduler with random completion latencies for the asynchronous copies and MMAs,
 and checks on every run:
@@ -64,8 +66,9 @@ class Bar:
 class Model:
     """One CTA's roles over a list of items (index, (segment length, split))."""
 
-    def __init__(self, items, ST, QBUF, BN, seed, mistake=None):
+    def __init__(self, items, ST, QBUF, BN, seed, mistake=None, defer=False):
         self.rng = random.Random(seed)
+        self.defer = defer
         self.items, self.ST, self.QBUF, self.BN, self.mistake = items, ST, QBUF, BN, mistake
         B = lambda n, c: [Bar(f"{n}{i}", c) for i in range(max(ST, 2))]
         self.q_full, self.q_empty = B("q_full", 1), B("q_empty", 2)
@@ -302,9 +305,19 @@ class Model:
             t += n_kv
 
     # ------------------------------------------------------------ softmax warps and warp 3
+    def _write_out(self, grp, idx, n_kv):
+        """A two-tile item's output: O read (it must hold every tile of the item), then o_free."""
+        self.O_readers[grp] += 1
+        assert self.O[grp] == (idx, frozenset(range(n_kv))), f"O {self.O[grp]}"
+        yield (self.always, 0)                  # the epilogue's reads take time
+        assert self.O[grp] == (idx, frozenset(range(n_kv))), f"O changed while read {self.O[grp]}"
+        self.O_readers[grp] -= 1
+        self.o_free[grp].arrive()
+
     def softmax(self, grp, warp):
         BN = self.BN
         p_cnt = 0
+        pend = None                             # a two-tile item whose output is not written yet
         for ev in self.items_taken():
             if ev[0] != "item":
                 yield ev
@@ -328,16 +341,22 @@ class Model:
                     self.P[grp] = (idx, j)
                 self.p_full[grp].arrive()
                 p_cnt += 1
+                # the previous item's output, after the first P of this one (its last P.V is done)
+                if pend is not None:
+                    yield from self._write_out(grp, *pend)
+                    pend = None
                 j += dj
             if not split:
-                yield (self.pv_done[grp], p_cnt - 1)
-                self.O_readers[grp] += 1
-                assert self.O[grp] == (idx, frozenset(range(n_kv))), f"O {self.O[grp]}"
-                yield (self.always, 0)          # the epilogue's reads take time
-                assert self.O[grp] == (idx, frozenset(range(n_kv))), f"O changed while read {self.O[grp]}"
-                self.O_readers[grp] -= 1
-                self.o_free[grp].arrive()
+                if self.defer:                  # head_dim 128: written after the next item's first P
+                    pend = (idx, n_kv)
+                else:                           # other head dims: written at once
+                    yield (self.pv_done[grp], p_cnt - 1)
+                    yield from self._write_out(grp, idx, n_kv)
                 continue
+            if pend is not None:                # a split item without a tile of this group
+                yield (self.pv_done[grp], p_cnt - 1)
+                yield from self._write_out(grp, *pend)
+                pend = None
             n1 = n_kv >> 1
             if grp == 0 or n1 > 0:
                 yield (self.pv_done[grp], p_cnt - 1)
@@ -359,6 +378,9 @@ class Model:
             else:
                 self.merges[(grp, warp)] = ph + 1
             self.o_free[grp].arrive()
+        if pend is not None:                    # the last item's output
+            yield (self.pv_done[grp], p_cnt - 1)
+            yield from self._write_out(grp, *pend)
 
     def warp3(self):
         for ev in self.items_taken():
@@ -415,10 +437,11 @@ def random_case(seed):
     return items, ST, QBUF, BN
 
 
-def test_protocol_holds_over_random_layouts_and_timings():
+@pytest.mark.parametrize("defer", [False, True])
+def test_protocol_holds_over_random_layouts_and_timings(defer):
     for seed in range(400):
         items, ST, QBUF, BN = random_case(seed)
-        Model(items, ST, QBUF, BN, seed).run()
+        Model(items, ST, QBUF, BN, seed, defer=defer).run()
 
 
 @pytest.mark.parametrize("mistake,expect", [
