@@ -122,6 +122,11 @@ LENGTH_CASES = [
     ([300, 400, 100, 513, 640, 2000], 16, 80),
     ([300, 1, 257, 511, 512, 513, 130], 16, 128),
     ([129, 200, 700, 96, 1100], 12, 64),
+    # tiny segments with an odd head count or one head: the tiny kernel's one-head items, beside
+    # the two-head items the even head counts above take
+    ([17, 64, 3, 40], 3, 96),
+    ([33, 48, 64, 16, 1], 5, 80),
+    ([5, 40, 64, 1], 1, 32),
 ]
 
 
