@@ -333,9 +333,11 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
         e = launch_attn_long(a, max_items(T, H, B, sp.bm_long / 2), sms, stall_v(), s);
         if (e != cudaSuccess) return VIT_ERR_CUDA;
     }
-    // segments of at most tiny_max tokens on the tiny-segment kernel (launched only when that
-    // class can be non-empty)
-    if (sp.tiny_max > 0) e = launch_attn_tiny(a, (int64_t)H * B, sms, s);
+    // segments of at most tiny_max tokens on the tiny-segment kernel, launched only when that
+    // class can be non-empty: the host knows the shortest segment only for one packed segment
+    // (T tokens) and for uniform segments (T / B each); an empty launch still costs ~6 us
+    const int64_t shortest = padded ? 0 : (!cu_seqlens ? T / B : (B == 1 ? T : 0));
+    if (sp.tiny_max > 0 && shortest <= sp.tiny_max) e = launch_attn_tiny(a, (int64_t)H * B, sms, s);
     return from_cuda(e);
 }
 
