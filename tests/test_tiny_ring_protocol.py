@@ -79,7 +79,7 @@ def simulate(lengths, D, seed, mistake=None, HG=1):
         pending.pop(0)
 
 
-@pytest.mark.parametrize("D,HG", [(32, 1), (32, 2), (64, 1), (80, 1), (80, 2), (96, 1), (96, 2), (128, 1)])
+@pytest.mark.parametrize("D,HG", [(32, 1), (32, 2), (64, 1), (80, 1), (80, 2), (80, 4), (96, 1), (96, 2), (128, 1)])
 def test_ring_never_overlaps_live_items(D, HG):
     rng = random.Random(D * 8 + HG)
     for seed in range(60):
@@ -94,7 +94,7 @@ def test_ring_never_overlaps_live_items(D, HG):
 
 
 def test_largest_item_fits_the_empty_ring():
-    for D, HG in [(32, 2), (64, 1), (80, 2), (96, 2), (128, 1)]:
+    for D, HG in [(32, 2), (64, 1), (80, 2), (80, 4), (96, 2), (128, 1)]:
         assert 3 * tile_bytes(D, TM // 16, HG) <= RING
 
 

@@ -328,6 +328,7 @@ vit_status_t varlen_attn_impl(const void *q, const void *k, const void *v, int64
     }
     // a segment can only be long when the bound allows it
     const int64_t longest = (cu_seqlens || padded) ? (int64_t)max_seqlen : T / B;
+    a.max_len = longest;
     if (longest > sp.tiny_max) {
         // split items cover bm_long / 2 rows, so that many more items may exist
         e = launch_attn_long(a, max_items(T, H, B, sp.bm_long / 2), sms, stall_v(), s);

@@ -113,6 +113,7 @@ struct AttnArgs {
     float *lse;                 // fp32 [T, H] natural-log sum of exp(scale * s) per row, or NULL
     int64_t T;
     int H, D;
+    int64_t max_len;            // upper bound on every segment's length (max_seqlen, or T / B uniform)
     int64_t q_stride, k_stride, v_stride, out_stride;   // token strides, elements
     float scale_log2;           // softmax scale * log2(e)
     const WsHeader *hdr;
