@@ -13,7 +13,7 @@
 // per SM:
 //   - one work item = one segment and HG consecutive heads (2 at head_dim 32,
 //     80 and 96 when the head count is even, 4 at head_dim 80 when no segment
-//     can exceed 16 tokens and the head count allows, else 1), so that a token's
+//     can exceed 24 tokens and the head count allows, else 1), so that a token's
 //     row of the item is HG * D * 2 contiguous bytes; one persistent CTA per SM;
 //   - a producer warp copies each item's Q, K and V with tiled TMA loads of 16
 //     rows each into the next free bytes of the ring: an item takes ceil16(L)
@@ -446,13 +446,14 @@ cudaError_t launch_hg(const AttnArgs &a, int64_t max_items, int num_sms, cudaStr
 
 // Heads per item: as many as make the copied rows wide (several heads side by side) while the
 // row still falls under a conflict-free swizzle, and divide the head count. Four at head_dim 80
-// when no segment can exceed 16 tokens (an item is then at most 30 KB, so the ring still holds
-// seven; measured 1.7x faster than two on 4-16-token images, slower on 16-64-token ones).
+// when no segment can exceed 24 tokens (an item is then at most 61 KB; measured 1.6x faster
+// than two on 4-16-token images and 1.1x on 9-24-token ones, even at 17-32 tokens and slower
+// on 16-64-token ones, whose items would leave the ring room for two).
 template <int D>
 cudaError_t launch_d(const AttnArgs &a, int64_t max_items, int num_sms, cudaStream_t stream)
 {
     if constexpr (D == 80) {
-        if (a.H % 4 == 0 && a.max_len <= 16) return launch_hg<D, 4>(a, max_items, num_sms, stream);
+        if (a.H % 4 == 0 && a.max_len <= 24) return launch_hg<D, 4>(a, max_items, num_sms, stream);
     }
     if constexpr (D == 32 || D == 80 || D == 96) {
         if (a.H % 2 == 0) return launch_hg<D, 2>(a, max_items, num_sms, stream);
