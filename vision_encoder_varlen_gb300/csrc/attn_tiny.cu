@@ -1,6 +1,6 @@
 // Tiny-segment varlen attention (segments of at most 64 tokens) on warp-level MMA.
 //
-// Same result as the other two attention kernels: for each (segment, head) the
+// Same result as the tcgen05 long-segment kernel: for each (segment, head) the
 // plain softmax(scale * q k^T) v over that segment's keys only (vLLM Dots
 // vision_attention page, VisionAttentionV2.forward / VisionAttention.forward),
 // softmax in fp32, P rounded to bf16 for the P.V product, fp32 accumulation,
@@ -74,7 +74,8 @@ template <int D, bool FQ, int HG> struct TinyCfg {
     // 64-byte span, and an odd number of 128-byte spans under the 128-byte span.
     static constexpr int SLABS = D == 128 ? 2 : 1;
     static constexpr int SLAB_BYTES = HG * D * 2 / SLABS;
-    static constexpr int W = SLAB_BYTES == 160 ? 16 : ((SLAB_BYTES == 64 || SLAB_BYTES == 192 || SLAB_BYTES == 320) ? 32 : 64);
+    static constexpr int W =
+        SLAB_BYTES == 160 ? 16 : ((SLAB_BYTES == 64 || SLAB_BYTES == 192 || SLAB_BYTES == 320) ? 32 : 64);
     static constexpr int CHUNKS = SLAB_BYTES / (2 * W);
     static constexpr uint32_t SWZ = W == 16 ? 1 : (W == 32 ? 3 : 7);   // 16-byte chunk bits flipped
     static constexpr int RING = 220 * 1024;                      // bytes of the item ring
@@ -125,7 +126,8 @@ __device__ __forceinline__ uint32_t keep_keys(uint32_t b, int k0, int L) {
 template <int D, bool FQ, int HG>
 __global__ void __launch_bounds__(TinyCfg<D, FQ, HG>::THREADS, 1)
 attn_tiny_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out, int64_t out_stride, float *__restrict__ lse, int H,
+                 const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out, int64_t out_stride,
+                 float *__restrict__ lse, int H,
                  float scale_log2, const WsHeader *__restrict__ hdr, const Item *__restrict__ items,
                  int32_t *__restrict__ status, const rope::QRope qr)
 {
@@ -415,8 +417,10 @@ template <int D, int HG>
 cudaError_t launch_hg(const AttnArgs &a, int64_t max_items, int num_sms, cudaStream_t stream)
 {
     using C = TinyCfg<D, false, HG>;
-    constexpr size_t smem = C::SMEM;
-    static_assert(C::SMEM + sizeof(TinyShared) <= 227 * 1024, "shared memory budget");
+    using CF = TinyCfg<D, true, HG>;                     // the variant that rotates raw Q
+    const size_t smem = a.fuse_q ? CF::SMEM : C::SMEM;
+    static_assert(C::SMEM + sizeof(TinyShared) <= 227 * 1024 && CF::SMEM + sizeof(TinyShared) <= 227 * 1024,
+                  "shared memory budget");
     // [T, H*D] rows seen as {W elements, H*D/W chunks, T rows}; boxes of {W, CHUNKS, 16}
     if ((int64_t)a.H * D % C::W != 0) return cudaErrorInvalidValue;
     CUtensorMap maps[3];
@@ -429,7 +433,7 @@ cudaError_t launch_hg(const AttnArgs &a, int64_t max_items, int num_sms, cudaStr
         if (!encode_tiled_map(&maps[t], ptrs[t], 3, dims, st, box, C::W * 2)) return cudaErrorInvalidValue;
     }
     auto kern = a.fuse_q ? attn_tiny_kernel<D, true, HG> : attn_tiny_kernel<D, false, HG>;
-    const int threads = a.fuse_q ? TinyCfg<D, true, HG>::THREADS : C::THREADS;
+    const int threads = a.fuse_q ? CF::THREADS : C::THREADS;
     static DeviceOnce once[2];                           // per fused-Q variant
     cudaError_t e = once[a.fuse_q ? 1 : 0].run([&] {
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
