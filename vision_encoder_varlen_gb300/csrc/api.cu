@@ -393,8 +393,8 @@ vit_status_t vit_varlen_attn(const void *q, const void *k, const void *v, int64_
 {
     TraceRange trace("vit_varlen_attn");
     return varlen_attn_impl(q, k, v, T, H, D, q_stride, k_stride, v_stride, nullptr, cu_seqlens, nullptr, nullptr, B,
-                            max_seqlen, scale, out, out_stride, nullptr, nullptr, workspace, workspace_bytes, status_dev,
-                            stream);
+                            max_seqlen, scale, out, out_stride, nullptr, nullptr, workspace, workspace_bytes,
+                            status_dev, stream);
 }
 
 vit_status_t vit_varlen_attn_ex(const void *q, const void *k, const void *v, int64_t T, int H, int D,

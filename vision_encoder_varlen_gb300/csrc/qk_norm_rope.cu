@@ -107,7 +107,8 @@ qk_norm_rope_kernel(const __nv_bfloat16 *q_in, __nv_bfloat16 *q_out,
                 act[k] = row_ok && c < CHUNKS;
                 tt_[k] = tt;
                 which_[k] = which;
-                const __nv_bfloat16 *src = (which ? k_in + t * k_in_stride : q_in + t * q_in_stride) + (int64_t)h * D + c * 8;
+                const __nv_bfloat16 *src =
+                    (which ? k_in + t * k_in_stride : q_in + t * q_in_stride) + (int64_t)h * D + c * 8;
                 dst[k] = (which ? k_out + t * k_out_stride : q_out + t * q_out_stride) + (int64_t)h * D + c * 8;
                 if (act[k]) {
                     va[k] = *reinterpret_cast<const uint4 *>(src);
