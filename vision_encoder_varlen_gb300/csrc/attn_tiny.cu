@@ -64,6 +64,9 @@ template <int D, bool FQ, int HG> struct TinyCfg {
     // in 32-column chunks to stay below).
     static constexpr int GROUPS = 3;
     static constexpr int PV_CHUNK = (D == 128 || (D == 96 && HG == 1)) ? 4 : D / 8;   // 8-column blocks
+    // output stores of 8 bytes per lane (pairs of lanes swap a word) except at head_dim 128, where
+    // the 32-column P.V chunks measured faster with the plain 4-byte stores between them
+    static constexpr bool PAIR_STORES = D != 128;
     static constexpr int CONSUMERS = 4 * GROUPS;
     static constexpr int THREADS = 32 * (CONSUMERS + 1);
     // An item is one segment and HG consecutive heads. A tensor tile of an item holds its rows
@@ -396,16 +399,43 @@ attn_tiny_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 // this warp's reads of the ring are done after the last chunk of its last unit
                 if (c0 + NC >= DN && u + kStep >= units) release();
+                if constexpr (C::PAIR_STORES) {
+                    // two 8-column blocks at a time: the lanes of a pair (tig, tig ^ 1) swap one word
+                    // so that the even lane holds four consecutive columns of block j and the odd
+                    // lane four of block j + 1; a quad then writes 32 contiguous bytes of a row (one
+                    // whole sector) with one 8-byte store per lane instead of two 4-byte stores
+                    static_assert(NC % 2 == 0 && DN % 2 == 0, "blocks are stored in pairs");
+                    const bool odd = tig & 1;
 #pragma unroll
-                for (int j = 0; j < NC; ++j) {
-                    if (c0 + j < DN) {
-                        const int col = (c0 + j) * 8 + tig * 2;
-                        if (r0 < L)
-                            *reinterpret_cast<uint32_t *>(oh + (int64_t)(seg0 + r0) * out_stride + col) =
-                                pack_bf16(o[j][0] * inv0, o[j][1] * inv0);
-                        if (r1 < L)
-                            *reinterpret_cast<uint32_t *>(oh + (int64_t)(seg0 + r1) * out_stride + col) =
-                                pack_bf16(o[j][2] * inv1, o[j][3] * inv1);
+                    for (int j = 0; j < NC; j += 2) {
+                        if (c0 + j < DN) {
+                            const uint32_t a0 = pack_bf16(o[j][0] * inv0, o[j][1] * inv0);
+                            const uint32_t a1 = pack_bf16(o[j][2] * inv1, o[j][3] * inv1);
+                            const uint32_t b0 = pack_bf16(o[j + 1][0] * inv0, o[j + 1][1] * inv0);
+                            const uint32_t b1 = pack_bf16(o[j + 1][2] * inv1, o[j + 1][3] * inv1);
+                            const uint32_t t0 = __shfl_xor_sync(0xffffffffu, odd ? a0 : b0, 1);
+                            const uint32_t t1 = __shfl_xor_sync(0xffffffffu, odd ? a1 : b1, 1);
+                            const int col = (c0 + j + (odd ? 1 : 0)) * 8 + (tig & 2) * 2;
+                            if (r0 < L)
+                                *reinterpret_cast<uint2 *>(oh + (int64_t)(seg0 + r0) * out_stride + col) =
+                                    odd ? make_uint2(t0, b0) : make_uint2(a0, t0);
+                            if (r1 < L)
+                                *reinterpret_cast<uint2 *>(oh + (int64_t)(seg0 + r1) * out_stride + col) =
+                                    odd ? make_uint2(t1, b1) : make_uint2(a1, t1);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < NC; ++j) {
+                        if (c0 + j < DN) {
+                            const int col = (c0 + j) * 8 + tig * 2;
+                            if (r0 < L)
+                                *reinterpret_cast<uint32_t *>(oh + (int64_t)(seg0 + r0) * out_stride + col) =
+                                    pack_bf16(o[j][0] * inv0, o[j][1] * inv0);
+                            if (r1 < L)
+                                *reinterpret_cast<uint32_t *>(oh + (int64_t)(seg0 + r1) * out_stride + col) =
+                                    pack_bf16(o[j][2] * inv1, o[j][3] * inv1);
+                        }
                     }
                 }
             }
