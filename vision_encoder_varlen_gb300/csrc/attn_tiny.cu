@@ -35,7 +35,11 @@
 //     zeros past the last token): keys past it get score -inf by a select, V rows
 //     past it are zeroed in registers before the P.V product, and query rows past
 //     it are never stored, so no other segment's values (finite or not) enter a
-//     result.
+//     result;
+//   - the output leaves in whole 16-byte pieces of a row: the MMA accumulator
+//     gives each lane two columns of every 8-column block, and the four lanes
+//     of a quad exchange words (two shuffle stages) so that each holds one
+//     block (not at head_dim 128, where 4-byte stores measured faster).
 // Every wait is bounded: one that gives up records VIT_ERR_TIMEOUT, all roles
 // leave their loops, and the producer waits (with a short limit) for its copies
 // in flight before the CTA exits.
@@ -64,9 +68,9 @@ template <int D, bool FQ, int HG> struct TinyCfg {
     // in 32-column chunks to stay below).
     static constexpr int GROUPS = 3;
     static constexpr int PV_CHUNK = (D == 128 || (D == 96 && HG == 1)) ? 4 : D / 8;   // 8-column blocks
-    // output stores of 8 bytes per lane (pairs of lanes swap a word) except at head_dim 128, where
-    // the 32-column P.V chunks measured faster with the plain 4-byte stores between them
-    static constexpr bool PAIR_STORES = D != 128;
+    // output stores of 16 bytes per lane (the lanes of a quad exchange words) except at head_dim
+    // 128, where the 32-column P.V chunks measured faster with plain 4-byte stores between them
+    static constexpr bool WIDE_STORES = D != 128;
     static constexpr int CONSUMERS = 4 * GROUPS;
     static constexpr int THREADS = 32 * (CONSUMERS + 1);
     // An item is one segment and HG consecutive heads. A tensor tile of an item holds its rows
@@ -399,30 +403,57 @@ attn_tiny_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 // this warp's reads of the ring are done after the last chunk of its last unit
                 if (c0 + NC >= DN && u + kStep >= units) release();
-                if constexpr (C::PAIR_STORES) {
-                    // two 8-column blocks at a time: the lanes of a pair (tig, tig ^ 1) swap one word
-                    // so that the even lane holds four consecutive columns of block j and the odd
-                    // lane four of block j + 1; a quad then writes 32 contiguous bytes of a row (one
-                    // whole sector) with one 8-byte store per lane instead of two 4-byte stores
-                    static_assert(NC % 2 == 0 && DN % 2 == 0, "blocks are stored in pairs");
-                    const bool odd = tig & 1;
+                if constexpr (C::WIDE_STORES) {
+                    // the four lanes of a quad hold, per row, one word (two columns) of each 8-column
+                    // block; a 4 x 4 transpose across the quad (two shuffle stages) gives each lane a
+                    // whole block of a row, written with one 16-byte store; a trailing pair of blocks
+                    // (head_dim 80) swaps one word between the lanes of a pair for 8-byte stores
+                    static_assert(DN % NC == 0 && NC % 2 == 0, "whole chunks of paired blocks");
+                    const bool lo = tig & 1, hi = tig & 2;
+                    __nv_bfloat16 *row0 = oh + (int64_t)(seg0 + r0) * out_stride;
+                    __nv_bfloat16 *row1 = oh + (int64_t)(seg0 + r1) * out_stride;
+                    // x[i]: this lane's word of block j + i in one row; returns the words of block
+                    // j + tig in column order
+                    auto transpose4 = [&](uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3) {
+                        // lanes two apart swap halves: keep the columns of block pair `hi`
+                        const uint32_t k0 = hi ? x2 : x0, k1 = hi ? x3 : x1;
+                        const uint32_t g0 = __shfl_xor_sync(0xffffffffu, hi ? x0 : x2, 2);
+                        const uint32_t g1 = __shfl_xor_sync(0xffffffffu, hi ? x1 : x3, 2);
+                        // neighbours swap: z[m] = word of lane tig ^ m for block j + tig
+                        const uint32_t z1 = __shfl_xor_sync(0xffffffffu, lo ? k0 : k1, 1);
+                        const uint32_t z3 = __shfl_xor_sync(0xffffffffu, lo ? g0 : g1, 1);
+                        const uint32_t z0 = lo ? k1 : k0, z2 = lo ? g1 : g0;
+                        // y[e] = z[e ^ tig]
+                        const uint32_t w0 = lo ? z1 : z0, w1 = lo ? z0 : z1, w2 = lo ? z3 : z2, w3 = lo ? z2 : z3;
+                        return hi ? make_uint4(w2, w3, w0, w1) : make_uint4(w0, w1, w2, w3);
+                    };
 #pragma unroll
-                    for (int j = 0; j < NC; j += 2) {
-                        if (c0 + j < DN) {
-                            const uint32_t a0 = pack_bf16(o[j][0] * inv0, o[j][1] * inv0);
-                            const uint32_t a1 = pack_bf16(o[j][2] * inv1, o[j][3] * inv1);
-                            const uint32_t b0 = pack_bf16(o[j + 1][0] * inv0, o[j + 1][1] * inv0);
-                            const uint32_t b1 = pack_bf16(o[j + 1][2] * inv1, o[j + 1][3] * inv1);
-                            const uint32_t t0 = __shfl_xor_sync(0xffffffffu, odd ? a0 : b0, 1);
-                            const uint32_t t1 = __shfl_xor_sync(0xffffffffu, odd ? a1 : b1, 1);
-                            const int col = (c0 + j + (odd ? 1 : 0)) * 8 + (tig & 2) * 2;
-                            if (r0 < L)
-                                *reinterpret_cast<uint2 *>(oh + (int64_t)(seg0 + r0) * out_stride + col) =
-                                    odd ? make_uint2(t0, b0) : make_uint2(a0, t0);
-                            if (r1 < L)
-                                *reinterpret_cast<uint2 *>(oh + (int64_t)(seg0 + r1) * out_stride + col) =
-                                    odd ? make_uint2(t1, b1) : make_uint2(a1, t1);
+                    for (int j = 0; j + 4 <= NC; j += 4) {
+                        uint32_t x[2][4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            x[0][i] = pack_bf16(o[j + i][0] * inv0, o[j + i][1] * inv0);
+                            x[1][i] = pack_bf16(o[j + i][2] * inv1, o[j + i][3] * inv1);
                         }
+                        const uint4 y0 = transpose4(x[0][0], x[0][1], x[0][2], x[0][3]);
+                        const uint4 y1 = transpose4(x[1][0], x[1][1], x[1][2], x[1][3]);
+                        const int col = (c0 + j + tig) * 8;
+                        if (r0 < L) *reinterpret_cast<uint4 *>(row0 + col) = y0;
+                        if (r1 < L) *reinterpret_cast<uint4 *>(row1 + col) = y1;
+                    }
+                    if constexpr (NC % 4 == 2) {
+                        constexpr int j = NC - 2;
+                        const uint32_t a0 = pack_bf16(o[j][0] * inv0, o[j][1] * inv0);
+                        const uint32_t a1 = pack_bf16(o[j][2] * inv1, o[j][3] * inv1);
+                        const uint32_t b0 = pack_bf16(o[j + 1][0] * inv0, o[j + 1][1] * inv0);
+                        const uint32_t b1 = pack_bf16(o[j + 1][2] * inv1, o[j + 1][3] * inv1);
+                        const uint32_t t0 = __shfl_xor_sync(0xffffffffu, lo ? a0 : b0, 1);
+                        const uint32_t t1 = __shfl_xor_sync(0xffffffffu, lo ? a1 : b1, 1);
+                        const int col = (c0 + j + (lo ? 1 : 0)) * 8 + (tig & 2) * 2;
+                        if (r0 < L)
+                            *reinterpret_cast<uint2 *>(row0 + col) = lo ? make_uint2(t0, b0) : make_uint2(a0, t0);
+                        if (r1 < L)
+                            *reinterpret_cast<uint2 *>(row1 + col) = lo ? make_uint2(t1, b1) : make_uint2(a1, t1);
                     }
                 } else {
 #pragma unroll
