@@ -323,13 +323,15 @@ attn_tiny_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
             }
-            // softmax over the whole key range in one pass (log2 domain); keys past the end -> -inf
+            // softmax over the whole key range in one pass: the row max of the raw scores (the
+            // scale is positive), then p = 2^(s * scale*log2(e) - max * scale*log2(e)) with one FMA
+            // per score; keys past the end -> -inf
 #pragma unroll
             for (int nb = 0; nb < 8; ++nb)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c = nb * 8 + tig * 2 + (e & 1);
-                    const float x = c < L ? s[nb][e] * scale_log2 : -INFINITY;
+                    const float x = c < L ? s[nb][e] : -INFINITY;
                     s[nb][e] = x;
                     mx[e >> 1] = fmaxf(mx[e >> 1], x);
                 }
@@ -337,13 +339,14 @@ attn_tiny_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int r = 0; r < 2; ++r) {
                 mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
                 mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                mx[r] *= scale_log2;                         // the row max in the log2 domain
             }
 #pragma unroll
             for (int nb = 0; nb < 8; ++nb)
                 if (nb < 2 * n16)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float p = ex2(s[nb][e] - mx[e >> 1]);
+                        const float p = ex2(fmaf(s[nb][e], scale_log2, -mx[e >> 1]));
                         s[nb][e] = p;
                         l[e >> 1] += p;
                     }
