@@ -364,7 +364,8 @@ attn_tiny_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
                 l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
             }
-            const float inv0 = 1.f / l[0], inv1 = 1.f / l[1];
+            // l >= 1 (the row max contributes 2^0): the fast reciprocal is within an ulp or two
+            const float inv0 = __fdividef(1.f, l[0]), inv1 = __fdividef(1.f, l[1]);
             const int r0 = r_base + g, r1 = r0 + 8;
             if (lse && tig == 0) {                           // ln(sum exp(scale * s)) = (m + log2 l) ln 2
                 if (r0 < L) lse[(int64_t)(seg0 + r0) * H + head] = (mx[0] + log2f(l[0])) * 0.6931471805599453f;
