@@ -47,6 +47,8 @@
 #include "sm100.cuh"
 #include "warp_mma.cuh"
 
+#include <type_traits>
+
 namespace vit {
 namespace {
 
@@ -71,6 +73,10 @@ template <int D, bool FQ, int HG> struct TinyCfg {
     // output stores of 16 bytes per lane (the lanes of a quad exchange words) except at head_dim
     // 128, where the 32-column P.V chunks measured faster with plain 4-byte stores between them
     static constexpr bool WIDE_STORES = D != 128;
+    // one copy of a unit's code per count of 16-key groups: measured faster at head_dim 80 with
+    // several heads per item (16-64 tokens: -9 %, 9-24 tokens: -16 %), slower at 64 and 128, where
+    // the copies also no longer fit the registers without spilling
+    static constexpr bool PER_N16 = D == 80 && HG >= 2 && !FQ;
     static constexpr int CONSUMERS = 4 * GROUPS;
     static constexpr int THREADS = 32 * (CONSUMERS + 1);
     // An item is one segment and HG consecutive heads. A tensor tile of an item holds its rows
@@ -297,184 +303,201 @@ attn_tiny_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int u = u0; u < units; u += kStep) {
             const int rt = u / HG, hl = u - rt * HG;
             const int r_base = rt * 16, cq = hl * D, head = head0 + hl;
-            // the tile addresses are re-derived in each unit: hoisting the K and V fragment
-            // addresses out of the loop would hold dozens of registers across it
-            uint32_t sQ = sQ0, sK = sK0, sV = sV0;
-            asm volatile("" : "+r"(sQ), "+r"(sK), "+r"(sV));
-            float s[8][4];
-            float mx[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-            // S = Q K^T for 16 rows x up to 64 keys
+            // at head_dim 80 (several heads per item) the unit's code is compiled once per count of
+            // 16-key groups (1 to 4), so every loop over key groups has a fixed trip count; N16 = 0
+            // is the one copy for any count
+            auto unit = [&](auto n16c) {
+                constexpr int N16 = decltype(n16c)::value;
+                const int nk = N16 > 0 ? N16 : n16;
+                // the tile addresses are re-derived in each unit: hoisting the K and V fragment
+                // addresses out of the loop would hold dozens of registers across it
+                uint32_t sQ = sQ0, sK = sK0, sV = sV0;
+                asm volatile("" : "+r"(sQ), "+r"(sK), "+r"(sV));
+                float s[8][4];
+                float mx[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+                // S = Q K^T for 16 rows x up to 64 keys
 #pragma unroll
-            for (int nb = 0; nb < 8; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
+                for (int nb = 0; nb < 8; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                uint32_t a[4];
-                ldsm_x4(C::at(sQ, n16, r_base + (lane & 7) + ((lane >> 3) & 1) * 8, cq + kk * 16 + (lane >> 4) * 8),
-                        a[0], a[1], a[2], a[3]);
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    uint32_t a[4];
+                    ldsm_x4(C::at(sQ, nk, r_base + (lane & 7) + ((lane >> 3) & 1) * 8, cq + kk * 16 + (lane >> 4) * 8),
+                            a[0], a[1], a[2], a[3]);
 #pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    if (np < n16) {
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(C::at(sK, n16, np * 16 + (lane & 7) + (lane >> 4) * 8,
-                                      cq + kk * 16 + ((lane >> 3) & 1) * 8),
-                                b0, b1, b2, b3);
-                        mma16816(s[2 * np], a, b0, b1);
-                        mma16816(s[2 * np + 1], a, b2, b3);
+                    for (int np = 0; np < 4; ++np) {
+                        if (np < nk) {
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(C::at(sK, nk, np * 16 + (lane & 7) + (lane >> 4) * 8,
+                                          cq + kk * 16 + ((lane >> 3) & 1) * 8),
+                                    b0, b1, b2, b3);
+                            mma16816(s[2 * np], a, b0, b1);
+                            mma16816(s[2 * np + 1], a, b2, b3);
+                        }
                     }
                 }
-            }
-            // softmax over the whole key range in one pass: the row max of the raw scores (the
-            // scale is positive), then p = 2^(s * scale*log2(e) - max * scale*log2(e)) with one FMA
-            // per score; keys past the end -> -inf
+                // softmax over the whole key range in one pass: the row max of the raw scores (the
+                // scale is positive), then p = 2^(s * scale*log2(e) - max * scale*log2(e)) with one FMA
+                // per score; keys past the end -> -inf
 #pragma unroll
-            for (int nb = 0; nb < 8; ++nb)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = nb * 8 + tig * 2 + (e & 1);
-                    const float x = c < L ? s[nb][e] : -INFINITY;
-                    s[nb][e] = x;
-                    mx[e >> 1] = fmaxf(mx[e >> 1], x);
-                }
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                mx[r] *= scale_log2;                         // the row max in the log2 domain
-            }
-#pragma unroll
-            for (int nb = 0; nb < 8; ++nb)
-                if (nb < 2 * n16)
+                for (int nb = 0; nb < 8; ++nb)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float p = ex2(fmaf(s[nb][e], scale_log2, -mx[e >> 1]));
-                        s[nb][e] = p;
-                        l[e >> 1] += p;
+                        const int c = nb * 8 + tig * 2 + (e & 1);
+                        const float x = c < L ? s[nb][e] : -INFINITY;
+                        s[nb][e] = x;
+                        mx[e >> 1] = fmaxf(mx[e >> 1], x);
                     }
-            // P as bf16 A fragments, one per 16-key group (S is dead after this)
-            uint32_t pa[4][4];
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                pa[np][0] = pack_bf16(s[2 * np][0], s[2 * np][1]);
-                pa[np][1] = pack_bf16(s[2 * np][2], s[2 * np][3]);
-                pa[np][2] = pack_bf16(s[2 * np + 1][0], s[2 * np + 1][1]);
-                pa[np][3] = pack_bf16(s[2 * np + 1][2], s[2 * np + 1][3]);
-            }
+                for (int r = 0; r < 2; ++r) {
+                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                    mx[r] *= scale_log2;                         // the row max in the log2 domain
+                }
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-            }
-            // l >= 1 (the row max contributes 2^0): the fast reciprocal is within an ulp or two
-            const float inv0 = __fdividef(1.f, l[0]), inv1 = __fdividef(1.f, l[1]);
-            const int r0 = r_base + g, r1 = r0 + 8;
-            if (lse && tig == 0) {                           // ln(sum exp(scale * s)) = (m + log2 l) ln 2
-                if (r0 < L) lse[(int64_t)(seg0 + r0) * H + head] = (mx[0] + log2f(l[0])) * 0.6931471805599453f;
-                if (r1 < L) lse[(int64_t)(seg0 + r1) * H + head] = (mx[1] + log2f(l[1])) * 0.6931471805599453f;
-            }
-            __nv_bfloat16 *oh = out + (int64_t)head * D;
-            // O = P V over the 16-key groups of the segment, in chunks of NC 8-column blocks that
-            // are normalised and stored before the next: at the widest rows, 16 accumulators
-            // instead of D / 2 keep the unit within 128 registers
-            constexpr int NC = C::PV_CHUNK;
+                for (int nb = 0; nb < 8; ++nb)
+                    if (nb < 2 * nk)
 #pragma unroll
-            for (int c0 = 0; c0 < DN; c0 += NC) {
-                float o[NC][4];
-#pragma unroll
-                for (int j = 0; j < NC; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+                        for (int e = 0; e < 4; ++e) {
+                            const float p = ex2(fmaf(s[nb][e], scale_log2, -mx[e >> 1]));
+                            s[nb][e] = p;
+                            l[e >> 1] += p;
+                        }
+                // P as bf16 A fragments, one per 16-key group (S is dead after this)
+                uint32_t pa[4][4];
 #pragma unroll
                 for (int np = 0; np < 4; ++np) {
-                    if (np < n16) {
-                        const int row = np * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                        // fragments b0/b2 hold keys 16 np + 2 tig (+1), b1/b3 the same + 8
-                        const int k0 = np * 16 + 2 * tig, k1 = k0 + 8;
-                        const bool tail = np * 16 + 16 > L;
+                    pa[np][0] = pack_bf16(s[2 * np][0], s[2 * np][1]);
+                    pa[np][1] = pack_bf16(s[2 * np][2], s[2 * np][3]);
+                    pa[np][2] = pack_bf16(s[2 * np + 1][0], s[2 * np + 1][1]);
+                    pa[np][3] = pack_bf16(s[2 * np + 1][2], s[2 * np + 1][3]);
+                }
 #pragma unroll
-                        for (int j = 0; j < NC; j += 2) {
-                            if (c0 + j < DN) {
-                                uint32_t b0, b1, b2, b3;
-                                ldsm_x4_t(C::at(sV, n16, row, cq + (c0 + j) * 8 + (lane >> 4) * 8), b0, b1, b2, b3);
-                                if (tail) {
-                                    b0 = keep_keys(b0, k0, L);
-                                    b1 = keep_keys(b1, k1, L);
-                                    b2 = keep_keys(b2, k0, L);
-                                    b3 = keep_keys(b3, k1, L);
+                for (int r = 0; r < 2; ++r) {
+                    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+                    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+                }
+                // l >= 1 (the row max contributes 2^0): the fast reciprocal is within an ulp or two
+                const float inv0 = __fdividef(1.f, l[0]), inv1 = __fdividef(1.f, l[1]);
+                const int r0 = r_base + g, r1 = r0 + 8;
+                if (lse && tig == 0) {                           // ln(sum exp(scale * s)) = (m + log2 l) ln 2
+                    if (r0 < L) lse[(int64_t)(seg0 + r0) * H + head] = (mx[0] + log2f(l[0])) * 0.6931471805599453f;
+                    if (r1 < L) lse[(int64_t)(seg0 + r1) * H + head] = (mx[1] + log2f(l[1])) * 0.6931471805599453f;
+                }
+                __nv_bfloat16 *oh = out + (int64_t)head * D;
+                // O = P V over the 16-key groups of the segment, in chunks of NC 8-column blocks that
+                // are normalised and stored before the next: at the widest rows, 16 accumulators
+                // instead of D / 2 keep the unit within 128 registers
+                constexpr int NC = C::PV_CHUNK;
+#pragma unroll
+                for (int c0 = 0; c0 < DN; c0 += NC) {
+                    float o[NC][4];
+#pragma unroll
+                    for (int j = 0; j < NC; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+#pragma unroll
+                    for (int np = 0; np < 4; ++np) {
+                        if (np < nk) {
+                            const int row = np * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                            // fragments b0/b2 hold keys 16 np + 2 tig (+1), b1/b3 the same + 8
+                            const int k0 = np * 16 + 2 * tig, k1 = k0 + 8;
+                            const bool tail = np * 16 + 16 > L;
+#pragma unroll
+                            for (int j = 0; j < NC; j += 2) {
+                                if (c0 + j < DN) {
+                                    uint32_t b0, b1, b2, b3;
+                                    ldsm_x4_t(C::at(sV, nk, row, cq + (c0 + j) * 8 + (lane >> 4) * 8), b0, b1, b2, b3);
+                                    if (tail) {
+                                        b0 = keep_keys(b0, k0, L);
+                                        b1 = keep_keys(b1, k1, L);
+                                        b2 = keep_keys(b2, k0, L);
+                                        b3 = keep_keys(b3, k1, L);
+                                    }
+                                    mma16816(o[j], pa[np], b0, b1);
+                                    mma16816(o[j + 1], pa[np], b2, b3);
                                 }
-                                mma16816(o[j], pa[np], b0, b1);
-                                mma16816(o[j + 1], pa[np], b2, b3);
+                            }
+                        }
+                    }
+                    // this warp's reads of the ring are done after the last chunk of its last unit
+                    if (c0 + NC >= DN && u + kStep >= units) release();
+                    if constexpr (C::WIDE_STORES) {
+                        // the four lanes of a quad hold, per row, one word (two columns) of each 8-column
+                        // block; a 4 x 4 transpose across the quad (two shuffle stages) gives each lane a
+                        // whole block of a row, written with one 16-byte store; a trailing pair of blocks
+                        // (head_dim 80) swaps one word between the lanes of a pair for 8-byte stores
+                        static_assert(DN % NC == 0 && NC % 2 == 0, "whole chunks of paired blocks");
+                        const bool lo = tig & 1, hi = tig & 2;
+                        __nv_bfloat16 *row0 = oh + (int64_t)(seg0 + r0) * out_stride;
+                        __nv_bfloat16 *row1 = oh + (int64_t)(seg0 + r1) * out_stride;
+                        // x[i]: this lane's word of block j + i in one row; returns the words of block
+                        // j + tig in column order
+                        auto transpose4 = [&](uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3) {
+                            // lanes two apart swap halves: keep the columns of block pair `hi`
+                            const uint32_t k0 = hi ? x2 : x0, k1 = hi ? x3 : x1;
+                            const uint32_t g0 = __shfl_xor_sync(0xffffffffu, hi ? x0 : x2, 2);
+                            const uint32_t g1 = __shfl_xor_sync(0xffffffffu, hi ? x1 : x3, 2);
+                            // neighbours swap: z[m] = word of lane tig ^ m for block j + tig
+                            const uint32_t z1 = __shfl_xor_sync(0xffffffffu, lo ? k0 : k1, 1);
+                            const uint32_t z3 = __shfl_xor_sync(0xffffffffu, lo ? g0 : g1, 1);
+                            const uint32_t z0 = lo ? k1 : k0, z2 = lo ? g1 : g0;
+                            // y[e] = z[e ^ tig]
+                            const uint32_t w0 = lo ? z1 : z0, w1 = lo ? z0 : z1, w2 = lo ? z3 : z2, w3 = lo ? z2 : z3;
+                            return hi ? make_uint4(w2, w3, w0, w1) : make_uint4(w0, w1, w2, w3);
+                        };
+#pragma unroll
+                        for (int j = 0; j + 4 <= NC; j += 4) {
+                            uint32_t x[2][4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                x[0][i] = pack_bf16(o[j + i][0] * inv0, o[j + i][1] * inv0);
+                                x[1][i] = pack_bf16(o[j + i][2] * inv1, o[j + i][3] * inv1);
+                            }
+                            const uint4 y0 = transpose4(x[0][0], x[0][1], x[0][2], x[0][3]);
+                            const uint4 y1 = transpose4(x[1][0], x[1][1], x[1][2], x[1][3]);
+                            const int col = (c0 + j + tig) * 8;
+                            if (r0 < L) *reinterpret_cast<uint4 *>(row0 + col) = y0;
+                            if (r1 < L) *reinterpret_cast<uint4 *>(row1 + col) = y1;
+                        }
+                        if constexpr (NC % 4 == 2) {
+                            constexpr int j = NC - 2;
+                            const uint32_t a0 = pack_bf16(o[j][0] * inv0, o[j][1] * inv0);
+                            const uint32_t a1 = pack_bf16(o[j][2] * inv1, o[j][3] * inv1);
+                            const uint32_t b0 = pack_bf16(o[j + 1][0] * inv0, o[j + 1][1] * inv0);
+                            const uint32_t b1 = pack_bf16(o[j + 1][2] * inv1, o[j + 1][3] * inv1);
+                            const uint32_t t0 = __shfl_xor_sync(0xffffffffu, lo ? a0 : b0, 1);
+                            const uint32_t t1 = __shfl_xor_sync(0xffffffffu, lo ? a1 : b1, 1);
+                            const int col = (c0 + j + (lo ? 1 : 0)) * 8 + (tig & 2) * 2;
+                            if (r0 < L)
+                                *reinterpret_cast<uint2 *>(row0 + col) = lo ? make_uint2(t0, b0) : make_uint2(a0, t0);
+                            if (r1 < L)
+                                *reinterpret_cast<uint2 *>(row1 + col) = lo ? make_uint2(t1, b1) : make_uint2(a1, t1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < NC; ++j) {
+                            if (c0 + j < DN) {
+                                const int col = (c0 + j) * 8 + tig * 2;
+                                if (r0 < L)
+                                    *reinterpret_cast<uint32_t *>(oh + (int64_t)(seg0 + r0) * out_stride + col) =
+                                        pack_bf16(o[j][0] * inv0, o[j][1] * inv0);
+                                if (r1 < L)
+                                    *reinterpret_cast<uint32_t *>(oh + (int64_t)(seg0 + r1) * out_stride + col) =
+                                        pack_bf16(o[j][2] * inv1, o[j][3] * inv1);
                             }
                         }
                     }
                 }
-                // this warp's reads of the ring are done after the last chunk of its last unit
-                if (c0 + NC >= DN && u + kStep >= units) release();
-                if constexpr (C::WIDE_STORES) {
-                    // the four lanes of a quad hold, per row, one word (two columns) of each 8-column
-                    // block; a 4 x 4 transpose across the quad (two shuffle stages) gives each lane a
-                    // whole block of a row, written with one 16-byte store; a trailing pair of blocks
-                    // (head_dim 80) swaps one word between the lanes of a pair for 8-byte stores
-                    static_assert(DN % NC == 0 && NC % 2 == 0, "whole chunks of paired blocks");
-                    const bool lo = tig & 1, hi = tig & 2;
-                    __nv_bfloat16 *row0 = oh + (int64_t)(seg0 + r0) * out_stride;
-                    __nv_bfloat16 *row1 = oh + (int64_t)(seg0 + r1) * out_stride;
-                    // x[i]: this lane's word of block j + i in one row; returns the words of block
-                    // j + tig in column order
-                    auto transpose4 = [&](uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3) {
-                        // lanes two apart swap halves: keep the columns of block pair `hi`
-                        const uint32_t k0 = hi ? x2 : x0, k1 = hi ? x3 : x1;
-                        const uint32_t g0 = __shfl_xor_sync(0xffffffffu, hi ? x0 : x2, 2);
-                        const uint32_t g1 = __shfl_xor_sync(0xffffffffu, hi ? x1 : x3, 2);
-                        // neighbours swap: z[m] = word of lane tig ^ m for block j + tig
-                        const uint32_t z1 = __shfl_xor_sync(0xffffffffu, lo ? k0 : k1, 1);
-                        const uint32_t z3 = __shfl_xor_sync(0xffffffffu, lo ? g0 : g1, 1);
-                        const uint32_t z0 = lo ? k1 : k0, z2 = lo ? g1 : g0;
-                        // y[e] = z[e ^ tig]
-                        const uint32_t w0 = lo ? z1 : z0, w1 = lo ? z0 : z1, w2 = lo ? z3 : z2, w3 = lo ? z2 : z3;
-                        return hi ? make_uint4(w2, w3, w0, w1) : make_uint4(w0, w1, w2, w3);
                     };
-#pragma unroll
-                    for (int j = 0; j + 4 <= NC; j += 4) {
-                        uint32_t x[2][4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            x[0][i] = pack_bf16(o[j + i][0] * inv0, o[j + i][1] * inv0);
-                            x[1][i] = pack_bf16(o[j + i][2] * inv1, o[j + i][3] * inv1);
-                        }
-                        const uint4 y0 = transpose4(x[0][0], x[0][1], x[0][2], x[0][3]);
-                        const uint4 y1 = transpose4(x[1][0], x[1][1], x[1][2], x[1][3]);
-                        const int col = (c0 + j + tig) * 8;
-                        if (r0 < L) *reinterpret_cast<uint4 *>(row0 + col) = y0;
-                        if (r1 < L) *reinterpret_cast<uint4 *>(row1 + col) = y1;
-                    }
-                    if constexpr (NC % 4 == 2) {
-                        constexpr int j = NC - 2;
-                        const uint32_t a0 = pack_bf16(o[j][0] * inv0, o[j][1] * inv0);
-                        const uint32_t a1 = pack_bf16(o[j][2] * inv1, o[j][3] * inv1);
-                        const uint32_t b0 = pack_bf16(o[j + 1][0] * inv0, o[j + 1][1] * inv0);
-                        const uint32_t b1 = pack_bf16(o[j + 1][2] * inv1, o[j + 1][3] * inv1);
-                        const uint32_t t0 = __shfl_xor_sync(0xffffffffu, lo ? a0 : b0, 1);
-                        const uint32_t t1 = __shfl_xor_sync(0xffffffffu, lo ? a1 : b1, 1);
-                        const int col = (c0 + j + (lo ? 1 : 0)) * 8 + (tig & 2) * 2;
-                        if (r0 < L)
-                            *reinterpret_cast<uint2 *>(row0 + col) = lo ? make_uint2(t0, b0) : make_uint2(a0, t0);
-                        if (r1 < L)
-                            *reinterpret_cast<uint2 *>(row1 + col) = lo ? make_uint2(t1, b1) : make_uint2(a1, t1);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < NC; ++j) {
-                        if (c0 + j < DN) {
-                            const int col = (c0 + j) * 8 + tig * 2;
-                            if (r0 < L)
-                                *reinterpret_cast<uint32_t *>(oh + (int64_t)(seg0 + r0) * out_stride + col) =
-                                    pack_bf16(o[j][0] * inv0, o[j][1] * inv0);
-                            if (r1 < L)
-                                *reinterpret_cast<uint32_t *>(oh + (int64_t)(seg0 + r1) * out_stride + col) =
-                                    pack_bf16(o[j][2] * inv1, o[j][3] * inv1);
-                        }
-                    }
+            if constexpr (C::PER_N16) {
+                switch (n16) {
+                case 1: unit(std::integral_constant<int, 1>{}); break;
+                case 2: unit(std::integral_constant<int, 2>{}); break;
+                case 3: unit(std::integral_constant<int, 3>{}); break;
+                default: unit(std::integral_constant<int, 4>{}); break;
                 }
+            } else {
+                unit(std::integral_constant<int, 0>{});
             }
-        }
+}
     }
 }
 
