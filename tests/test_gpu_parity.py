@@ -127,6 +127,9 @@ LENGTH_CASES = [
     ([17, 64, 3, 40], 3, 96),
     ([33, 48, 64, 16, 1], 5, 80),
     ([5, 40, 64, 1], 1, 32),
+    # two-head items at head_dim 80, whose unit code is compiled per count of 16-key groups: every
+    # count (1-4) with full and ragged last groups
+    ([1, 16, 17, 31, 32, 33, 47, 48, 49, 63, 64, 24, 40, 8], 4, 80),
 ]
 
 
