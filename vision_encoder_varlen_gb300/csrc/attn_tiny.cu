@@ -486,7 +486,7 @@ attn_tiny_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         }
                     }
                 }
-                    };
+            };
             if constexpr (C::PER_N16) {
                 switch (n16) {
                 case 1: unit(std::integral_constant<int, 1>{}); break;
@@ -497,7 +497,7 @@ attn_tiny_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             } else {
                 unit(std::integral_constant<int, 0>{});
             }
-}
+        }
     }
 }
 
