@@ -500,12 +500,13 @@ def run_ours(args, rank, world, local):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "overlap": "step i+1's upload and step i's download on two copy streams run during compute"}
 
-    # ---- the other workloads of the study, each measured alone in this run (one GPU only)
+    # ---- the other workloads of the study, each measured alone in this run (one GPU only), and
+    # the short-segment workload (4096 images of 16-64 tokens) that the tiny-segment kernel serves
     per_config = None
     if world == 1 and args.config == 5 and not args.no_per_config:
         peaks, peaks_src = load_peaks()
         per_config = {str(i): per_config_entry(vit, i, args, rank, device, stream, flush_buf, peaks, peaks_src)
-                      for i in (1, 2, 3, 4)}
+                      for i in (1, 2, 3, 4, 7)}
 
     if rank != 0:
         return
@@ -617,7 +618,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-per-config", action="store_true",
-                    help="skip the per-workload block (workloads 1-4 measured after the headline workload 5)")
+                    help="skip the per-workload block (workloads 1-4 and the short-segment workload 7, measured "
+                         "after the headline workload 5)")
     ap.add_argument("--sweep-split", action="store_true",
                     help="time both attention kernels over bands of segment lengths and exit")
     ap.add_argument("--short-max", type=int, default=None,
