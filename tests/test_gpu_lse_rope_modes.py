@@ -69,6 +69,9 @@ LSE_CASES = [
     ([5, 3000, 7], 2, 80),
     ([200, 33, 96, 17], 4, 96),
     ([7, 9, 2100], 2, 64),
+    # two-head tiny items at head_dim 80 over every count of 16-key groups (the tiny kernel's unit
+    # code is compiled per count there)
+    ([1, 16, 17, 31, 33, 48, 49, 64, 24, 40], 4, 80),
 ]
 
 
@@ -87,6 +90,22 @@ def test_lse_parity_lengths(lengths, H, D, split):
     # the plain call writes the same output bits
     out2 = vit.varlen_attn(q, k, v, torch.from_numpy(w.cu_seqlens).cuda(), w.max_seqlen)
     assert torch.equal(out, out2)
+
+
+def test_lse_four_head_tiny_items(split):
+    """A segment bound of at most 24 tokens at head_dim 80 (head count divisible by four) makes
+    the tiny-segment kernel take four heads per item: its lse rows match the oracle and, bit for
+    bit, those of the two-head items a loose bound gives."""
+    w = wl.from_lengths([4, 16, 9, 1, 12, 24, 7, 3, 17], 8, 80)
+    t = w.tensors()
+    q, k, v = (t[n].cuda() for n in ("q", "k", "v"))
+    cu = torch.from_numpy(w.cu_seqlens).cuda()
+    out4, lse4 = vit.varlen_attn(q, k, v, cu, 24, return_lse=True)
+    out2, lse2 = vit.varlen_attn(q, k, v, cu, 131072, return_lse=True)
+    assert torch.equal(out4, out2) and torch.equal(lse4, lse2)
+    ref, ref_lse = oracle.attention(*_widen(t), w.cu_seqlens, return_lse=True)
+    assert_close(out4, ref, what="four-head items")
+    _assert_lse(lse4, ref_lse, "four-head items")
 
 
 def test_lse_explicit_scale_and_zero_q(split):
